@@ -1,0 +1,239 @@
+"""Pins of the oracle's whole path: hand-worked examples, the dequantisation
+error bound, the two-writer statistic of the pages, a float64 brute force on
+tiny inputs, the page layout, strided inputs and the error bits."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _brute import pipeline as brute_pipeline
+from _run import SENTINEL, cache_views, code_distance, fresh_cache, run_oracle_k, run_oracle_qk
+
+
+def _expand(spec):
+    """'64*[1.0] + 64*[-1.0]' -> list (the fixture's compact notation)."""
+    out = []
+    for part in spec.split("+"):
+        n, lst = part.strip().split("*", 1)
+        items = [v.strip() for v in lst.strip().strip("[]").split(",")]
+        out += int(n) * [int(v, 16) if v.startswith("0x") else float(v) for v in items]
+    return out
+
+
+@pytest.fixture(scope="module")
+def worked(golden_dir):
+    with open(os.path.join(golden_dir, "worked_examples.json")) as f:
+        return json.load(f)
+
+
+def _single_k(kvals, cos, sin, gamma, beta, eps, style, page_size=64, num_pages=1, slot=0,
+              pos=0):
+    k = synth.to_bf16_bits(np.array(kvals, np.float32))
+    assert np.array_equal(synth.bf16_bits_to_f32(k), np.array(kvals, np.float32))
+    cos_t = np.array([[1.0] * 32, cos * 32], np.float32)
+    sin_t = np.array([[0.0] * 32, sin * 32], np.float32)
+    cache = np.full(num_pages * page_size * 132, SENTINEL, np.uint8)
+    err, ke = oracle.k_prepare_store(
+        k, 128, np.array([pos], np.int64), np.array([slot], np.int64), cos_t, sin_t, 32, 2,
+        np.full(128, gamma, np.float32), np.full(128, beta, np.float32), eps, cache,
+        num_pages, page_size, 64, style)
+    assert err == 0
+    return cache, int(ke[0])
+
+
+def test_worked_k_identity(worked):
+    ex = worked["k_identity"]
+    y = oracle.layernorm(np.array(_expand(ex["k"]), np.float32), np.ones(128, np.float32),
+                         np.zeros(128, np.float32), ex["eps"])[0]
+    assert y[0] == np.float32(ex["expect_y"]) and y[127] == -np.float32(ex["expect_y"])
+    for style in (oracle.NEOX, oracle.GPTJ):
+        cache, e = _single_k(_expand(ex["k"]), [1.0], [0.0], 1.0, 0.0, ex["eps"], style, pos=0)
+        assert e == ex["expect_exp"]
+        assert list(cache[:128]) == _expand(ex["expect_codes"])
+        assert cache[64 * 128:64 * 128 + 4].view(np.float32)[0] == np.float32(2.0 ** e)
+
+
+def test_worked_k_quarter_turn(worked):
+    ex = worked["k_quarter_turn"]
+    for style, key in ((oracle.NEOX, "expect_codes_neox"), (oracle.GPTJ, "expect_codes_gptj")):
+        cache, e = _single_k(_expand(ex["k"]), ex["cos"], ex["sin"], 1.0, 0.0, ex["eps"], style,
+                             pos=1)
+        assert e == ex["expect_exp"]
+        assert list(cache[:128]) == _expand(ex[key]), style
+
+
+def test_worked_qk_fold_and_slot(worked):
+    ex = worked["qk_fold"]
+    kx = worked["k_identity"]
+    H = ex["H"]
+    q = np.stack([synth.to_bf16_bits(np.array(_expand(s), np.float32)) for s in ex["q"]])
+    for h, s in enumerate(ex["q"]):
+        assert np.array_equal(synth.bf16_bits_to_f32(q[h]), np.array(_expand(s), np.float32))
+    k = synth.to_bf16_bits(np.array(_expand(kx["k"]), np.float32))
+    w = synth.to_bf16_bits(np.array(ex["w"], np.float32))
+    P, NP = ex["page_size"], ex["num_pages"]
+    cache = np.full(NP * P * 132, SENTINEL, np.uint8)
+    q_fp8 = np.zeros((1, H, 128), np.uint8)
+    weights = np.zeros((1, H), np.float32)
+    err, qe, ke = oracle.qk_prepare_store(
+        q.reshape(-1), H * 128, 128, k, 128, w, H, np.array([0], np.int64),
+        np.array([ex["slot"]], np.int64), np.ones((1, 32), np.float32),
+        np.zeros((1, 32), np.float32), 32, 1, np.ones(128, np.float32),
+        np.zeros(128, np.float32), kx["eps"], ex["softmax_scale"], q_fp8, weights, cache,
+        NP, P, H, 64, oracle.NEOX)
+    assert err == 0
+    assert list(qe[0]) == ex["expect_q_exp"]
+    for h in range(H):
+        assert list(q_fp8[0, h]) == _expand(ex["expect_q_codes"][h]), h
+    assert list(weights[0]) == [np.float32(v) for v in ex["expect_weights"]]
+    lo, hi = ex["expect_code_bytes"]
+    sb, sbytes = ex["expect_scale_bytes"]
+    assert list(cache[lo:hi]) == _expand(kx["expect_codes"])
+    assert list(cache[sb:sb + 4]) == sbytes
+    untouched = np.ones(cache.size, bool)
+    untouched[lo:hi] = False
+    untouched[sb:sb + 4] = False
+    assert np.all(cache[untouched] == SENTINEL)
+
+
+def _half_ulp_e4m3(m):
+    """Half the E4M3 spacing around magnitude m (m <= 448)."""
+    E = np.floor(np.log2(np.maximum(m, 2.0 ** -6)))
+    return 0.5 * 2.0 ** (E - 3)
+
+
+def test_dequantisation_error_within_half_step():
+    rng = np.random.default_rng(12)
+    dec = oracle.e4m3_decode(np.arange(256, dtype=np.uint8)).astype(np.float64)
+    for scale in (1e-3, 1.0, 37.0, 1e4):
+        for _ in range(40):
+            z = (rng.standard_t(3, 128) * scale).astype(np.float32)
+            codes, e = oracle.quantize_vector(z)
+            v = z.astype(np.float64) * 2.0 ** -e
+            assert np.max(np.abs(v)) <= 448.0
+            err = np.abs(dec[codes] - v)
+            assert np.all(err <= _half_ulp_e4m3(np.abs(v)))
+            # the scale is the smallest one that fits: at 2^(e-1) the row overflows
+            assert max(np.max(np.abs(z)), np.float32(1e-4)) > 448.0 * 2.0 ** (e - 1)
+
+
+def test_two_writer_statistic(golden_dir):
+    """The unfused (bf16-intermediate) writer vs the fused one: scales equal
+    on almost every row, codes differ by at most one step on a small fraction
+    of elements, and the fused codes are the closer ones to a float64 truth
+    (sglang PR "Fuse the DSA indexer Q/K rope + quant + K-cache write",
+    Accuracy, note on the two K-cache writers)."""
+    note = {}
+    with open(os.path.join(golden_dir, "two_writer_note.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                k, v = line.split()
+                note[k] = float(v)
+    page_frac = note["differing"] / note["elements"]
+    inp = synth.make_decode(seed=21, T=2048, H=1, style=synth.NEOX)
+    fused = run_oracle_k(inp)
+    unfused = run_oracle_k(inp, bf16_intermediate=True)
+    assert fused["err"] == 0 and unfused["err"] == 0
+    same_scale = fused["k_exp"] == unfused["k_exp"]
+    assert same_scale.mean() >= 0.99
+    codes_f, _ = cache_views(inp, fused["cache"])
+    codes_u, _ = cache_views(inp, unfused["cache"])
+    rows = inp.slots[same_scale]
+    d = code_distance(codes_f[rows], codes_u[rows])
+    assert d.max() <= note["max_code_distance"]
+    frac = (d > 0).mean()
+    # A bf16 rounding changes the E4M3 code only for values within half a bf16
+    # step (2^-8 of the binade) of an E4M3 midpoint (steps of 2^-3) whose tie
+    # goes the other way: about 1/32 of elements.  The pages saw 15 / 5248 on
+    # model data; here the rate is bounded by the window estimate.
+    assert 0 < frac <= 1.5 / 32, (frac, page_frac)
+    # fused is closer to the float64 truth on most differing elements
+    from _brute import bf16, rope64
+    dec = oracle.e4m3_decode(np.arange(256, dtype=np.uint8)).astype(np.float64)
+    closer = total = 0
+    for t in np.flatnonzero(same_scale)[:400]:
+        s = inp.slots[t]
+        diff = np.flatnonzero(codes_f[s] != codes_u[s])
+        if diff.size == 0:
+            continue
+        x = bf16(inp.k[t])
+        mu = x.mean()
+        y = (x - mu) / np.sqrt(((x - mu) ** 2).mean() + float(np.float32(inp.eps)))
+        y = y * inp.gamma + inp.beta
+        p = inp.positions[t]
+        z = rope64(y, inp.cos[p], inp.sin[p], 64, inp.style) * 2.0 ** -fused["k_exp"][t]
+        ef = np.abs(dec[codes_f[s, diff]] - z[diff])
+        eu = np.abs(dec[codes_u[s, diff]] - z[diff])
+        closer += int(np.sum(ef < eu))
+        total += diff.size
+    assert total > 0 and closer >= 0.5 * total
+
+
+@pytest.mark.parametrize("style", [synth.NEOX, synth.GPTJ])
+def test_bruteforce_tiny(style):
+    inp = synth.make_tiny(seed=3, T=3, H=2, style=style, fused_kw=True)
+    out = run_oracle_qk(inp)
+    assert out["err"] == 0
+    qc, qe, wt, kc, ke = brute_pipeline(inp)
+    assert np.array_equal(out["q_exp"], qe)
+    assert np.array_equal(out["k_exp"], ke)
+    assert code_distance(out["q_fp8"], qc).max() <= 1
+    assert (code_distance(out["q_fp8"], qc) > 0).mean() < 0.01
+    assert np.all(np.abs(out["weights"] - wt) <= 1e-6 * np.abs(wt))
+    codes, scales = cache_views(inp, out["cache"])
+    assert code_distance(codes[inp.slots], kc).max() <= 1
+    assert np.array_equal(scales[inp.slots], np.exp2(ke).astype(np.float32))
+    # every byte outside the written slots keeps the sentinel
+    mask = np.ones(inp.cache_bytes, bool)
+    P = inp.page_size
+    for s in inp.slots:
+        p, o = divmod(int(s), P)
+        base = p * P * 132
+        mask[base + o * 128: base + o * 128 + 128] = False
+        mask[base + P * 128 + 4 * o: base + P * 128 + 4 * o + 4] = False
+    assert np.all(out["cache"][mask] == SENTINEL)
+
+
+def test_strided_equals_contiguous():
+    a = synth.make_tiny(seed=4, T=4, H=8, fused_kw=True)
+    b = synth.make_tiny(seed=4, T=4, H=8, fused_kw=False)
+    assert np.array_equal(a.k, b.k) and np.array_equal(a.w, b.w)
+    oa, ob = run_oracle_qk(a), run_oracle_qk(b)
+    for key in ("q_fp8", "weights", "cache"):
+        assert np.array_equal(oa[key], ob[key]), key
+
+
+def test_k_only_writes_same_cache_as_qk():
+    inp = synth.make_tiny(seed=5, fused_kw=True)
+    assert np.array_equal(run_oracle_qk(inp)["cache"], run_oracle_k(inp)["cache"])
+
+
+def test_error_bits_skip_writes():
+    inp = synth.make_tiny(seed=6, T=4, H=8)
+    inp.positions = inp.positions.copy()
+    inp.slots = inp.slots.copy()
+    inp.positions[1] = inp.max_position      # bad position -> token skipped
+    inp.slots[2] = inp.num_pages * inp.page_size  # bad slot -> cache write skipped
+    out = run_oracle_qk(inp)
+    assert out["err"] == 3
+    assert np.all(out["q_fp8"][1] == 0) and np.all(out["weights"][1] == 0)
+    assert np.any(out["q_fp8"][2] != 0)
+    ref = run_oracle_qk(synth.make_tiny(seed=6, T=4, H=8))
+    codes, _ = cache_views(inp, out["cache"])
+    rcodes, _ = cache_views(inp, ref["cache"])
+    for t in (0, 3):
+        assert np.array_equal(codes[inp.slots[t]], rcodes[inp.slots[t]])
+    written = {int(inp.slots[0]), int(inp.slots[3])}
+    for s in range(inp.num_pages * inp.page_size):
+        if s not in written:
+            assert np.all(codes[s] == SENTINEL)
+
+
+def test_empty_batch():
+    inp = synth.make_tiny(seed=7)
+    out = run_oracle_qk(inp, T=0)
+    assert out["err"] == 0
+    assert np.all(out["cache"] == SENTINEL)
