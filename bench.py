@@ -1,0 +1,501 @@
+"""Benchmark of the DSA indexer fused Q/K prepare-and-store on GB300.
+
+One step = one fused call over the prefill workload (T = 8192 tokens of one
+sequence, H = 64 indexer heads, D = 128, rope_dim = 64 NeoX, slots contiguous
+in 128 pages of 64): the whole hot path (RoPE on q and k, LayerNorm on k,
+e4m3 + ue8m0 quantisation, gate-weight fold, index-K cache store) in one
+kernel launch.  Prints ONE JSON line (rank 0):
+
+  value      tokens/s over all ranks, inputs resident in HBM (two alternating
+             input sets of 2 x 210 MB, so no step reads the previous one's data
+             from the 129 MB L2)
+  e2e        the same through the public Python API with pinned host buffers:
+             host->device copy of q, k|w, positions and slots, the call, and
+             device->host copy of (q_fp8, weights), all inside the timed region
+  roofline   algorithmic bytes per launch / launch time vs the measured HBM
+             copy bandwidth; traffic = DRAM bytes per launch from the committed
+             ncu summary when it was taken on the current kernel source
+  decode     us per call at the decode shapes (T = 64, H = 64, GPT-J; and
+             T in {1, 8, 32, 64, 256}, H = 32, NeoX), graph-replayed (21 calls on
+             21 distinct input sets per graph, L2 flushed before each replay)
+             and eager
+  cpu_baseline  the oracle (plain C, one core) on a bounded sample
+
+``--impl reference`` times the oracle instead (the CPU statement of the path),
+on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s + achieved HBM GB/s (% of peak) prefill; µs/call at decode T=1..64"
+WORKLOAD = "prefill T=8192 H=64 D=128 rope_dim=64 NeoX, 128 pages x 64 (contiguous slots)"
+PROFILE = os.path.join(ROOT, "profiles", "dsa_prepare_store_prefill_T8192_H64.md")
+KERNEL_SRC = os.path.join(ROOT, "prep_token_gb300", "csrc", "dsa_prep.cu")
+L2_FLUSH_BYTES = 256 << 20
+GRAPH_STEPS = 50
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def profile_traffic():
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source has changed since it was captured."""
+    if not os.path.exists(PROFILE):
+        return None
+    text = open(PROFILE).read()
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    if not (m_b and m_h):
+        return None
+    cur = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+    return float(m_b.group(1)) if cur == m_h.group(1) else None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling around a timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.out, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.out):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.out):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.out)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        num = lambda v: float(v) if re.match(r"^[0-9.]+$", v) else None
+        sm = [num(r[1]) for r in rows]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows]
+        pmax = max([p for p in pw if p is not None], default=None)
+        # "under load": samples drawing at least half the peak power seen
+        loaded = [s for s, p in zip(sm, pw)
+                  if s is not None and p is not None and pmax and p >= 0.5 * pmax]
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": pmax, "samples": len(rows), "samples_under_load": len(loaded),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- our arm
+
+def _dev_inputs(inp, dev):
+    import torch
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    kw = bf16(inp.kw)
+    d = dict(q=bf16(inp.q), kw=kw, k=kw[:, :128], w=kw[:, 128:])
+    for n, key in (("positions", "positions"), ("slots", "slots"), ("cos", "cos"),
+                   ("sin", "sin"), ("gamma", "gamma"), ("beta", "beta")):
+        d[key] = torch.from_numpy(getattr(inp, n)).to(dev)
+    d["cache"] = torch.zeros(inp.cache_bytes, dtype=torch.uint8, device=dev)
+    d["q_out"] = torch.empty((inp.T, inp.H, 128), dtype=torch.float8_e4m3fn, device=dev)
+    d["w_out"] = torch.empty((inp.T, inp.H), dtype=torch.float32, device=dev)
+    return d
+
+
+def _call(dp, inp, d, stream, T=None, k_only=False):
+    if k_only:
+        dp.dsa_indexer_k_prepare_store(
+            d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
+            inp.eps, d["cache"], inp.page_size, inp.rope_dim, inp.style,
+            max_position=inp.max_position, stream=stream, num_tokens=T)
+        return
+    dp.dsa_indexer_qk_prepare_store(
+        d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
+        d["beta"], inp.eps, inp.softmax_scale, d["cache"], inp.page_size, inp.rope_dim,
+        inp.style, q_fp8_out=d["q_out"], weights_out=d["w_out"],
+        max_position=inp.max_position, stream=stream, num_tokens=T)
+
+
+def _decode_timings(dp, torch, dev, make, label, reps=30, layers=21, k_only_too=False):
+    """us/call: a graph of `layers` sequential calls on distinct input sets,
+    replayed `reps` times with an L2 flush before each replay (only the replay
+    is timed); a single-call graph; eager back-to-back calls."""
+    sets = []
+    for i in range(layers):
+        inp = make(i)
+        sets.append((inp, _dev_inputs(inp, dev)))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    out = {"T": sets[0][0].T, "H": sets[0][0].H, "style": "gptj" if sets[0][0].style else "neox"}
+    modes = [("qk", False)] + ([("k_only", True)] if k_only_too else [])
+    for name, k_only in modes:
+        with torch.cuda.stream(stream):
+            for inp, d in sets:          # warm-up outside capture
+                _call(dp, inp, d, stream, k_only=k_only)
+        stream.synchronize()
+        res = {}
+        for n_layers in (layers, 1):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for inp, d in sets[:n_layers]:
+                    _call(dp, inp, d, stream, k_only=k_only)
+            times = []
+            for _ in range(reps):
+                with torch.cuda.stream(stream):
+                    flush.fill_(1)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                stream.synchronize()
+                times.append(e0.elapsed_time(e1) * 1000.0 / n_layers)
+            res[f"graph{n_layers}_us"] = {"median": statistics.median(times), "best": min(times)}
+            del g
+        # eager: back-to-back calls through the Python binding
+        times = []
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                flush.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for inp, d in sets:
+                    _call(dp, inp, d, stream, k_only=k_only)
+                e1.record(stream)
+                stream.synchronize()
+                times.append(e0.elapsed_time(e1) * 1000.0 / len(sets))
+        res["eager_us"] = {"median": statistics.median(times), "best": min(times)}
+        out[name] = res
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import prep_token_gb300 as dp
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dp.library()
+    peaks, peak_kind = measured_peaks()
+
+    # two input sets, alternated, so consecutive steps never share L2 lines
+    sets = []
+    for i in range(2):
+        inp = synth.make_prefill(seed=3 + 1000 * rank + i)
+        sets.append((inp, _dev_inputs(inp, dev)))
+    T, H = sets[0][0].T, sets[0][0].H
+    algo_bytes = synth.algorithmic_bytes(T, H)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        inp, d = sets[i & 1]
+        _call(dp, inp, d, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+    # The K timed steps are replayed from CUDA graphs (GRAPH_STEPS launches per
+    # graph, plus one graph for the remainder) so the host's per-call Python
+    # cost never gaps the device; every step is still one full launch.
+    per_graph = min(GRAPH_STEPS, args.steps)
+    n_rep, rem = divmod(args.steps, per_graph)
+    graphs = []
+    for n, reps in ((per_graph, n_rep), (rem, 1)):
+        if n and reps:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    step(i)
+            graphs.append((g, reps))
+    with torch.cuda.stream(stream):
+        for g, _ in graphs:
+            g.replay()
+    stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for g, reps in graphs:
+                for _ in range(reps):
+                    g.replay()
+            e1.record(stream)
+        stream.synchronize()
+    del graphs
+    torch.cuda.synchronize(dev)
+    elapsed_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        torch.distributed.barrier()
+    ms_per_step = elapsed_ms / args.steps
+    value = world * T * args.steps / (elapsed_ms / 1000.0)
+    launch_us = ms_per_step * 1000.0
+    achieved = algo_bytes / (launch_us * 1e-6) / 1e9
+
+    # end to end through the public API, host buffers, copies inside the region
+    inp0, d0 = sets[0]
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_q = pin(inp0.q.view(np.int16)).view(torch.bfloat16)
+    h_kw = pin(inp0.kw.view(np.int16)).view(torch.bfloat16)
+    h_pos, h_slots = pin(inp0.positions), pin(inp0.slots)
+    h_qo = torch.empty((T, H, 128), dtype=torch.uint8).pin_memory()
+    h_wo = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(50, args.steps))
+
+    def e2e_step():
+        d0["q"].copy_(h_q, non_blocking=True)
+        d0["kw"].copy_(h_kw, non_blocking=True)
+        d0["positions"].copy_(h_pos, non_blocking=True)
+        d0["slots"].copy_(h_slots, non_blocking=True)
+        _call(dp, inp0, d0, stream)
+        h_qo.copy_(d0["q_out"].view(torch.uint8), non_blocking=True)
+        h_wo.copy_(d0["w_out"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        f1.record(stream)
+    stream.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = h_q.numel() * 2 + h_kw.numel() * 2 + h_pos.numel() * 8 + h_slots.numel() * 8
+    d2h = h_qo.numel() + h_wo.numel() * 4
+
+    decode = None
+    if rank == 0 and not args.no_decode:
+        decode = {"c2_decode_T64_H64_gptj": _decode_timings(
+            dp, torch, dev, lambda i: synth.make_decode(seed=1 + 100 * i), "c2", k_only_too=True)}
+        for Tn in (1, 8, 32, 64, 256):
+            decode[f"sweep_T{Tn}_H32"] = _decode_timings(
+                dp, torch, dev, lambda i, Tn=Tn: synth.make_sweep(Tn, seed=2 + 100 * i), "c3")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(sets[0][0], budget_s=args.cpu_seconds)
+
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "io_dtype": "bf16 in; e4m3 codes + fp32 ue8m0 scales + fp32 weights out",
+        "data": "synthetic (seeded N(0,1) bf16, positions 0..8191, contiguous slots)",
+        "config": {"workload": WORKLOAD, "T": T, "H": H, "head_dim": 128, "rope_dim": 64,
+                   "rope_style": "neox", "page_size": 64, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: two alternating input sets of "
+                         f"{algo_bytes / 1e6:.0f} MB per call"},
+        "gb_per_s": achieved,
+        "hbm_frac": achieved / peaks["hbm_gbs"],
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "peak_kind": f"{peak_kind} (torch bf16 copy, read+write)",
+                     "algorithmic_bytes_per_launch": algo_bytes,
+                     "launch_us": launch_us,
+                     "traffic": profile_traffic(),
+                     "nominal_frac_8tbs": achieved / 8000.0},
+        "e2e": {"value": world * T * e2e_steps / (e2e_ms / 1000.0), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+        "decode": decode,
+        "cpu_baseline": cpu,
+    }
+
+
+# ----------------------------------------------------------------- oracle
+
+def _oracle_call(inp, lo, hi, cache, q_fp8, weights):
+    import oracle
+    kw = inp.kw[lo:hi]
+    return oracle.qk_prepare_store(
+        np.ascontiguousarray(inp.q[lo:hi]).reshape(-1), inp.q_stride_t, inp.q_stride_h,
+        np.ascontiguousarray(kw).reshape(-1), inp.k_stride_t,
+        np.ascontiguousarray(kw).reshape(-1)[128:], inp.w_stride_t,
+        np.ascontiguousarray(inp.positions[lo:hi]), np.ascontiguousarray(inp.slots[lo:hi]),
+        inp.cos, inp.sin, inp.cs_stride, inp.max_position, inp.gamma, inp.beta, inp.eps,
+        inp.softmax_scale, q_fp8, weights, cache, inp.num_pages, inp.page_size, inp.H,
+        inp.rope_dim, inp.style)
+
+
+def cpu_baseline(inp, budget_s=10.0):
+    """The oracle, as it stands, on one host core, over consecutive chunks of
+    the prefill workload until `budget_s` of CPU time has been spent."""
+    import oracle
+    oracle.build()
+    chunk = 256
+    cache = np.zeros(inp.cache_bytes, np.uint8)
+    q_fp8 = np.zeros((chunk, inp.H, 128), np.uint8)
+    weights = np.zeros((chunk, inp.H), np.float32)
+    done, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        lo = done % inp.T
+        hi = min(inp.T, lo + chunk)
+        _oracle_call(inp, lo, hi, cache, q_fp8, weights)
+        done += hi - lo
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} tokens of the prefill workload (chunks of {chunk}), "
+                      f"{dt:.1f} s on one host core"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import synth
+    import oracle
+    oracle.build()
+    inp = synth.make_prefill(seed=3)
+    cache = np.zeros(inp.cache_bytes, np.uint8)
+    # calibrate, then size each step's sample so the whole run stays ~2 minutes
+    q_fp8 = np.zeros((inp.T, inp.H, 128), np.uint8)
+    weights = np.zeros((inp.T, inp.H), np.float32)
+    t0 = time.perf_counter()
+    _oracle_call(inp, 0, 32, cache, q_fp8, weights)
+    per_tok = (time.perf_counter() - t0) / 32
+    total_steps = args.steps + args.warmup
+    sample = int(max(1, min(inp.T, 120.0 / max(total_steps, 1) / per_tok)))
+    for i in range(args.warmup):
+        lo = (i * sample) % inp.T
+        _oracle_call(inp, lo, min(inp.T, lo + sample), cache, q_fp8, weights)
+    toks, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        lo = ((args.warmup + i) * sample) % inp.T
+        hi = min(inp.T, lo + sample)
+        _oracle_call(inp, lo, hi, cache, q_fp8, weights)
+        toks += hi - lo
+    dt = time.perf_counter() - t0
+    value = toks / dt
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1000 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "T": inp.T, "H": inp.H},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{sample} tokens of the prefill workload per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local_rank = _env_int("LOCAL_RANK", 0)
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl")
+        out = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

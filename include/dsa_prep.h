@@ -1,0 +1,151 @@
+/*
+ * dsa_prep.h -- C ABI of the DSA indexer Q/K prepare-and-store for GB300
+ * (sm_103a).
+ *
+ * What the calls compute (page title, section):
+ *   sglang PR "[AMD] [GLM5] Fuse the DSA indexer Q/K rope + quant + K-cache
+ *   write", Motivation: per layer and step the indexer applies rope to q and
+ *   k, LayerNorm to k, an fp8 quant to each, the head-gate scale, and writes
+ *   the index-K cache, all of which one fused launch does.  Modifications: the
+ *   fused call returns the (q_fp8, weights) contract, honours the token count
+ *   and the sliced out_cache_loc of the graph split-op, needs fp32 LayerNorm
+ *   parameters, reads cos and sin as separate [max_position, rope_dim/2]
+ *   rows, and a k-only prepare-and-store serves the dense decode fast path.
+ *   Accuracy (note on the two K-cache writers): fp32 goes to fp8 in one step,
+ *   with ue8m0 (power-of-two) scales.
+ *   vllm PR "[ROCm][Perf] Enable fused indexer-Q RoPE+quant kernel for
+ *   DeepSeek/GLM sparse attention", Summary and Kernel-level evidence: on the
+ *   query side RoPE, FP8 (ue8m0) quantisation and the weight-scale fold are one
+ *   launch.
+ *
+ * Per token t (D = 128, r = rope_dim):
+ *   k:  y = LayerNorm(k[t]) with fp32 gamma/beta (biased variance, eps inside
+ *       the root); RoPE on y[0:r); e_k = the smallest integer with
+ *       max(amax(y), 1e-4) <= 448 * 2^e_k; codes = e4m3_rne(y * 2^-e_k);
+ *       the 128 codes and the fp32 scale 2^e_k go to slot out_cache_loc[t].
+ *   q:  for every head h: RoPE on q[t,h,0:r); e_q and codes as above
+ *       (no LayerNorm) -> q_fp8[t,h,:];
+ *       weights[t,h] = w[t,h] * 2^e_q[t,h] * softmax_scale * H^-0.5.
+ *   RoPE pairs: DSA_ROPE_NEOX (i, i + r/2), DSA_ROPE_GPTJ (2i, 2i + 1), both
+ *   with frequency index i; a' = a*c - b*s, b' = b*c + a*s with c, s the
+ *   fp32 cos/sin at (position, i), evaluated as fma(a, c, -(b*s)) and
+ *   fma(b, c, a*s) with the products rounded to fp32.  Dims >= r pass through.
+ *   fp32 -> e4m3 is round-to-nearest-even, saturating at +-448.
+ *
+ * Index-K cache layout: num_pages pages of page_size * 132 bytes; page p
+ * holds page_size rows of 128 e4m3 codes, then page_size fp32 scales.  Slot s
+ * is row s % page_size of page s / page_size.
+ *
+ * Conventions shared by every call:
+ *   - Pointers are DEVICE pointers owned by the caller; the library allocates
+ *     nothing, keeps no state between calls and caches no pointer or table
+ *     contents (a replaced cos/sin cache is read afresh on the next call).
+ *   - Strides are in elements.  The innermost dimension of q, k and w is
+ *     contiguous.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  No call synchronises the host, so every call can be
+ *     captured into a CUDA graph.  One kernel launch per call.
+ *   - Host-side checks: a bad argument returns a status other than DSA_OK and
+ *     launches nothing.  T == 0 returns DSA_OK and launches nothing.
+ *   - Device-side checks: a position outside [0, max_position) sets bit
+ *     DSA_DEVERR_POSITION of *err_flags and that token writes nothing (no
+ *     q_fp8 rows, weights or cache slot); a slot outside
+ *     [0, num_pages * page_size) sets DSA_DEVERR_SLOT and skips that token's
+ *     cache write.  err_flags may be NULL (then nothing is reported).  The
+ *     kernel never traps.  The caller clears *err_flags.
+ *   - Slots within one call must be distinct (two tokens writing one slot
+ *     race).  Inputs must not overlap outputs.
+ *   - Non-finite inputs give unspecified codes and scales.
+ */
+#ifndef DSA_PREP_H
+#define DSA_PREP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_NULL = 1,        /* a required pointer is NULL */
+  DSA_ERR_ALIGN = 2,       /* a pointer or stride breaks an alignment rule */
+  DSA_ERR_SHAPE = 3,       /* a negative or inconsistent size or stride */
+  DSA_ERR_UNSUPPORTED = 4, /* head_dim != 128, bad rope_dim or style, ... */
+  DSA_ERR_LAUNCH = 5       /* the CUDA launch itself failed */
+} dsa_status;
+
+typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
+
+#define DSA_HEAD_DIM 128
+#define DSA_DEVERR_POSITION 1
+#define DSA_DEVERR_SLOT 2
+
+/*
+ * Fused Q/K prepare-and-store: returns the (q_fp8, weights) contract and
+ * writes k's codes and scale into the index-K cache, in one launch.
+ *
+ *   q              bf16 [T, H, 128]; row strides q_stride_t, q_stride_h.
+ *                  16-byte aligned; both strides multiples of 8.
+ *   k              bf16 [T, 128]; row stride k_stride_t (multiple of 8);
+ *                  16-byte aligned.  May be a column slice of the fused
+ *                  k/weights projection output.
+ *   w              bf16 [T, H] gate weights; row stride w_stride_t >= H;
+ *                  2-byte aligned.
+ *   positions      int64 [T], 8-byte aligned.
+ *   out_cache_loc  int64 [T] cache slots (the live, possibly sliced, view).
+ *   cos_cache,     fp32 [max_position, >= rope_dim/2] each, row stride
+ *   sin_cache      cs_stride (multiple of 4); 16-byte aligned.  May be NULL
+ *                  when rope_dim == 0.
+ *   ln_gamma,      fp32 [128], 16-byte aligned; ln_eps > 0 (it sits inside
+ *   ln_beta        the square root).
+ *   softmax_scale  the caller's attention scale (DeepSeek-style indexers pass
+ *                  128^-0.5); H^-0.5 is applied here.
+ *   q_fp8_out      e4m3 bytes [T, H, 128], contiguous, 16-byte aligned.
+ *   weights_out    fp32 [T, H], contiguous, 4-byte aligned.
+ *   index_k_cache  num_pages * page_size * 132 bytes, 16-byte aligned;
+ *                  page_size a multiple of 4.
+ *   T >= 0, 1 <= H <= 4096, head_dim == 128, rope_dim in {0, 16, ..., 128},
+ *   rope_style a dsa_rope_style.
+ */
+dsa_status dsa_indexer_qk_prepare_store(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    const void* k, int64_t k_stride_t,
+    const void* w, int64_t w_stride_t,
+    const int64_t* positions, const int64_t* out_cache_loc,
+    const float* cos_cache, const float* sin_cache, int64_t cs_stride,
+    int64_t max_position,
+    const float* ln_gamma, const float* ln_beta, float ln_eps,
+    float softmax_scale,
+    void* q_fp8_out, float* weights_out,
+    void* index_k_cache, int64_t num_pages, int32_t page_size,
+    int32_t T, int32_t H, int32_t head_dim, int32_t rope_dim,
+    int32_t rope_style, int32_t* err_flags, void* stream);
+
+/*
+ * k-only prepare-and-store (the decode fast path of sglang PR "[AMD] [GLM5]
+ * Fuse the DSA indexer Q/K rope + quant + K-cache write", Modifications):
+ * the k side of dsa_indexer_qk_prepare_store alone, same arguments, same
+ * rules, same cache bytes.
+ */
+dsa_status dsa_indexer_k_prepare_store(
+    const void* k, int64_t k_stride_t,
+    const int64_t* positions, const int64_t* out_cache_loc,
+    const float* cos_cache, const float* sin_cache, int64_t cs_stride,
+    int64_t max_position,
+    const float* ln_gamma, const float* ln_beta, float ln_eps,
+    void* index_k_cache, int64_t num_pages, int32_t page_size,
+    int32_t T, int32_t head_dim, int32_t rope_dim, int32_t rope_style,
+    int32_t* err_flags, void* stream);
+
+/* A static, NUL-terminated description of a status code. */
+const char* dsa_status_string(dsa_status status);
+
+/* Library version, (major << 16) | minor. */
+int32_t dsa_prep_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_PREP_H */

@@ -1,0 +1,217 @@
+"""DSA indexer Q/K prepare-and-store on GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``libdsaprep.so`` (declared in
+``include/dsa_prep.h``): it checks tensor dtypes and devices, allocates the
+outputs the caller did not pass, and forwards data pointers, strides and the
+current CUDA stream.  Every step of the path runs in the library's kernels;
+there is no CPU or PyTorch fallback, and a missing library raises.
+
+What the calls compute follows the sglang PR "[AMD] [GLM5] Fuse the DSA
+indexer Q/K rope + quant + K-cache write" (Motivation, Modifications) and the
+vllm PR "[ROCm][Perf] Enable fused indexer-Q RoPE+quant kernel for
+DeepSeek/GLM sparse attention" (Summary): RoPE on q and k, LayerNorm on k,
+e4m3 quantisation with one power-of-two scale per 128 values, the gate-weight
+fold, and the paged index-K cache write.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB_PATH
+
+__all__ = [
+    "DsaError", "NEOX", "GPTJ", "HEAD_DIM", "DEVERR_POSITION", "DEVERR_SLOT",
+    "dsa_indexer_qk_prepare_store", "dsa_indexer_k_prepare_store", "dsa_status_string",
+    "library", "cache_bytes", "cache_views",
+]
+
+NEOX, GPTJ = 0, 1
+HEAD_DIM = 128
+DEVERR_POSITION, DEVERR_SLOT = 1, 2
+ROW_BYTES = HEAD_DIM + 4  # 128 codes + one fp32 scale per slot
+
+_STATUS = {0: "DSA_OK", 1: "DSA_ERR_NULL", 2: "DSA_ERR_ALIGN", 3: "DSA_ERR_SHAPE",
+           4: "DSA_ERR_UNSUPPORTED", 5: "DSA_ERR_LAUNCH"}
+
+
+class DsaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS.get(status, status)} ({dsa_status_string(status)})")
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; "
+                "g.build()'); there is no fallback implementation")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I64, I32, F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        lib.dsa_indexer_qk_prepare_store.argtypes = [
+            P, I64, I64, P, I64, P, I64, P, P, P, P, I64, I64, P, P, F32, F32, P, P, P, I64, I32,
+            I32, I32, I32, I32, I32, P, P]
+        lib.dsa_indexer_qk_prepare_store.restype = ctypes.c_int
+        lib.dsa_indexer_k_prepare_store.argtypes = [
+            P, I64, P, P, P, P, I64, I64, P, P, F32, P, I64, I32, I32, I32, I32, I32, P, P]
+        lib.dsa_indexer_k_prepare_store.restype = ctypes.c_int
+        lib.dsa_status_string.argtypes = [ctypes.c_int]
+        lib.dsa_status_string.restype = ctypes.c_char_p
+        lib.dsa_prep_version.argtypes = []
+        lib.dsa_prep_version.restype = ctypes.c_int32
+        _lib = lib
+    return _lib
+
+
+def dsa_status_string(status: int) -> str:
+    return library().dsa_status_string(status).decode()
+
+
+def cache_bytes(num_pages: int, page_size: int) -> int:
+    return num_pages * page_size * ROW_BYTES
+
+
+def cache_views(index_k_cache: torch.Tensor, page_size: int):
+    """(codes [slots, 128] uint8, scales [slots] fp32) views of a paged
+    index-K cache: page p = [page_size x 128 codes][page_size x fp32 scale]."""
+    flat = index_k_cache.reshape(-1).view(torch.uint8)
+    num_pages = flat.numel() // (page_size * ROW_BYTES)
+    pages = flat[: num_pages * page_size * ROW_BYTES].view(num_pages, page_size * ROW_BYTES)
+    codes = pages[:, : page_size * HEAD_DIM].reshape(num_pages * page_size, HEAD_DIM)
+    scales = pages[:, page_size * HEAD_DIM:].contiguous().view(torch.float32).reshape(-1)
+    return codes, scales
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype, dim: int | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device (no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name}: expected {dim} dims, got {tuple(t.shape)}")
+    if t.dim() and t.stride(-1) != 1 and t.shape[-1] > 1:
+        raise ValueError(f"{name}: innermost dimension must be contiguous")
+
+
+def _num_pages(index_k_cache: torch.Tensor, page_size: int) -> int:
+    if not index_k_cache.is_contiguous():
+        raise ValueError("index_k_cache must be contiguous")
+    nbytes = index_k_cache.numel() * index_k_cache.element_size()
+    if page_size < 1 or nbytes % (page_size * ROW_BYTES):
+        raise ValueError("index_k_cache size is not a whole number of pages")
+    return nbytes // (page_size * ROW_BYTES)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta,
+              index_k_cache, rope_dim):
+    _need(k, "k", torch.bfloat16, 2)
+    _need(positions, "positions", torch.int64, 1)
+    _need(out_cache_loc, "out_cache_loc", torch.int64, 1)
+    _need(ln_gamma, "ln_gamma", torch.float32, 1)
+    _need(ln_beta, "ln_beta", torch.float32, 1)
+    if not isinstance(index_k_cache, torch.Tensor) or not index_k_cache.is_cuda:
+        raise ValueError("index_k_cache must be a CUDA tensor")
+    if rope_dim:
+        _need(cos_cache, "cos_cache", torch.float32, 2)
+        _need(sin_cache, "sin_cache", torch.float32, 2)
+        if cos_cache.stride(0) != sin_cache.stride(0) or cos_cache.shape[0] != sin_cache.shape[0]:
+            raise ValueError("cos_cache and sin_cache must share rows and row stride")
+        return cos_cache.stride(0), cos_cache.shape[0]
+    return 0, 1 << 62
+
+
+def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, sin_cache,
+                                 ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
+                                 page_size, rope_dim=64, rope_style=NEOX, *, q_fp8_out=None,
+                                 weights_out=None, err_flags=None, num_tokens=None,
+                                 max_position=None, stream=None):
+    """Fused Q/K prepare-and-store (one kernel launch).
+
+    q [T, H, 128] bf16, k [T, 128] bf16, w [T, H] bf16 (row strides of any
+    view are honoured), positions/out_cache_loc [T] int64, cos/sin caches
+    [max_position, >= rope_dim/2] fp32, ln_gamma/ln_beta [128] fp32,
+    index_k_cache: a contiguous CUDA buffer of whole pages (written in place).
+    ``num_tokens`` limits the call to the first T live tokens (the graph
+    split-op contract); outputs are sized to it.  Returns (q_fp8 [T, H, 128]
+    float8_e4m3fn, weights [T, H] fp32)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(w, "w", torch.bfloat16, 2)
+    cs_stride, rows = _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
+                                ln_beta, index_k_cache, rope_dim)
+    T = q.shape[0] if num_tokens is None else int(num_tokens)
+    H = q.shape[1]
+    if q.shape[2] != HEAD_DIM:
+        raise ValueError("q: head_dim must be 128")
+    for name, t in (("k", k), ("w", w), ("positions", positions), ("out_cache_loc", out_cache_loc)):
+        if t.shape[0] < T:
+            raise ValueError(f"{name} has fewer than {T} rows")
+    if w.shape[1] != H:
+        raise ValueError("w must be [T, H]")
+    dev = q.device
+    if q_fp8_out is None:
+        q_fp8_out = torch.empty((T, H, HEAD_DIM), dtype=torch.float8_e4m3fn, device=dev)
+    if weights_out is None:
+        weights_out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if q_fp8_out.numel() < T * H * HEAD_DIM or not q_fp8_out.is_contiguous():
+        raise ValueError("q_fp8_out must be contiguous [T, H, 128]")
+    if weights_out.dtype != torch.float32 or not weights_out.is_contiguous() \
+            or weights_out.numel() < T * H:
+        raise ValueError("weights_out must be contiguous fp32 [T, H]")
+    max_position = rows if max_position is None else int(max_position)
+    st = library().dsa_indexer_qk_prepare_store(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), _ptr(w), w.stride(0),
+        _ptr(positions), _ptr(out_cache_loc), _ptr(cos_cache) if rope_dim else None,
+        _ptr(sin_cache) if rope_dim else None, cs_stride, max_position, _ptr(ln_gamma),
+        _ptr(ln_beta), float(ln_eps), float(softmax_scale), _ptr(q_fp8_out), _ptr(weights_out),
+        _ptr(index_k_cache), _num_pages(index_k_cache, page_size), page_size, T, H, HEAD_DIM,
+        rope_dim, int(rope_style), _ptr(err_flags), _stream(stream))
+    if st != 0:
+        raise DsaError(st, "dsa_indexer_qk_prepare_store")
+    return q_fp8_out[:T] if q_fp8_out.dim() == 3 else q_fp8_out, \
+        weights_out[:T] if weights_out.dim() == 2 else weights_out
+
+
+def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
+                                ln_beta, ln_eps, index_k_cache, page_size, rope_dim=64,
+                                rope_style=NEOX, *, err_flags=None, num_tokens=None,
+                                max_position=None, stream=None):
+    """k-only prepare-and-store (one kernel launch); writes the cache in place."""
+    cs_stride, rows = _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
+                                ln_beta, index_k_cache, rope_dim)
+    T = k.shape[0] if num_tokens is None else int(num_tokens)
+    if k.shape[1] != HEAD_DIM:
+        raise ValueError("k: head_dim must be 128")
+    for name, t in (("positions", positions), ("out_cache_loc", out_cache_loc)):
+        if t.shape[0] < T:
+            raise ValueError(f"{name} has fewer than {T} rows")
+    max_position = rows if max_position is None else int(max_position)
+    st = library().dsa_indexer_k_prepare_store(
+        _ptr(k), k.stride(0), _ptr(positions), _ptr(out_cache_loc),
+        _ptr(cos_cache) if rope_dim else None, _ptr(sin_cache) if rope_dim else None,
+        cs_stride, max_position, _ptr(ln_gamma), _ptr(ln_beta), float(ln_eps),
+        _ptr(index_k_cache), _num_pages(index_k_cache, page_size), page_size, T, HEAD_DIM,
+        rope_dim, int(rope_style), _ptr(err_flags), _stream(stream))
+    if st != 0:
+        raise DsaError(st, "dsa_indexer_k_prepare_store")

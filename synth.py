@@ -23,6 +23,7 @@ All bf16 tensors are produced by round-to-nearest-even from fp32 draws.
 from __future__ import annotations
 
 import dataclasses
+import functools
 from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
@@ -105,8 +106,10 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+@functools.lru_cache(maxsize=8)
 def rope_table(max_position: int, rope_dim: int, base: float = ROPE_BASE):
-    """cos/sin cache [max_position, rope_dim/2] fp32 (angles in float64)."""
+    """cos/sin cache [max_position, rope_dim/2] fp32 (angles in float64).
+    Cached per arguments: callers must not modify the arrays."""
     half = rope_dim // 2
     inv_freq = base ** (-(2.0 * np.arange(half, dtype=np.float64)) / rope_dim)
     theta = np.arange(max_position, dtype=np.float64)[:, None] * inv_freq[None, :]

@@ -1,0 +1,231 @@
+"""CUDA path vs the oracle, through the C ABI, on every workload shape:
+tiny, decode (GPT-J), the decode sweep, prefill and the heavy-tailed stress
+set at full size, plus ragged shapes, strided views, rope-cache replacement,
+the live-token slice, device error bits and CUDA-graph replay."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from _compare import assert_parity, compare
+from _gpu import SENTINEL, new_cache, run_k, run_qk, to_device
+from _run import cache_views, run_oracle_k, run_oracle_qk
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import prep_token_gb300 as dp
+    dp.library()
+
+
+def _check(inp, q_exact=True):
+    d = to_device(inp)
+    gpu = run_qk(inp, d)
+    ref = run_oracle_qk(inp)
+    rep = assert_parity(inp, gpu, ref, q_exact=q_exact)
+    gk = run_k(inp, d)
+    assert np.array_equal(gk["cache"], gpu["cache"]), "k-only and qk caches differ"
+    return rep
+
+
+@pytest.mark.parametrize("style", [synth.NEOX, synth.GPTJ])
+def test_tiny(style):
+    _check(synth.make_tiny(style=style))
+
+
+def test_decode_gptj():
+    _check(synth.make_decode())
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 64, 256])
+def test_decode_sweep(T):
+    _check(synth.make_sweep(T))
+
+
+def test_prefill_full_size():
+    _check(synth.make_prefill())
+
+
+@pytest.fixture(scope="module")
+def stress_neox():
+    return synth.make_stress(style=synth.NEOX)
+
+
+@pytest.mark.parametrize("style", [synth.NEOX, synth.GPTJ])
+def test_stress_full_size(stress_neox, style):
+    inp = stress_neox
+    inp.style = style
+    rep = _check(inp)
+    print(style, rep)
+
+
+@pytest.mark.parametrize("H", [1, 3, 5, 7, 13, 64, 100, 128])
+@pytest.mark.parametrize("T", [1, 3, 33, 517])
+def test_ragged_shapes(T, H):
+    _check(synth.make_decode(seed=T * 1000 + H, T=T, H=H, style=(T + H) % 2))
+
+
+@pytest.mark.parametrize("rope_dim", [0, 16, 32, 48, 96, 128])
+@pytest.mark.parametrize("style", [synth.NEOX, synth.GPTJ])
+def test_rope_dims(rope_dim, style):
+    inp = synth.make_decode(seed=rope_dim + 7, T=40, H=6, style=style)
+    cos, sin = synth.rope_table(inp.max_position, max(rope_dim, 2))
+    inp.rope_dim = rope_dim
+    inp.cos, inp.sin = cos, sin
+    _check(inp)
+
+
+@pytest.mark.parametrize("page_size", [4, 16, 64, 256])
+def test_page_sizes(page_size):
+    inp = synth.make_decode(seed=page_size, T=50, H=4)
+    inp.page_size = page_size
+    inp.num_pages = (4096 * 64) // page_size
+    _check(inp)
+
+
+def test_strided_equals_contiguous():
+    a = synth.make_tiny(seed=9, T=37, H=16, fused_kw=True)
+    b = synth.make_tiny(seed=9, T=37, H=16, fused_kw=False)
+    da, db = to_device(a), to_device(b)
+    ga, gb = run_qk(a, da), run_qk(b, db)
+    for key in ("q_fp8", "weights", "cache"):
+        assert np.array_equal(ga[key], gb[key]), key
+    # q with a padded head stride and padded token stride
+    qpad = torch.zeros((37, 16, 192), dtype=torch.bfloat16, device="cuda")
+    qpad[:, :, :128] = db["q"]
+    dc = dict(db)
+    dc["q"] = qpad[:, :, :128]
+    assert dc["q"].stride() == (16 * 192, 192, 1)
+    gc = run_qk(b, dc)
+    for key in ("q_fp8", "weights", "cache"):
+        assert np.array_equal(gc[key], gb[key]), key
+
+
+def test_rope_cache_replaced_between_calls():
+    """The library keeps no table pointer or contents: overwrite the cos/sin
+    cache in place and the next call follows it."""
+    a = synth.make_tiny(seed=10, T=16, H=4)
+    d = to_device(a)
+    g1 = run_qk(a, d)
+    cos2, sin2 = synth.rope_table(a.max_position, 64, base=500000.0)
+    d["cos"].copy_(torch.from_numpy(cos2))
+    d["sin"].copy_(torch.from_numpy(sin2))
+    g2 = run_qk(a, d)
+    a.cos, a.sin = cos2, sin2
+    assert_parity(a, g2, run_oracle_qk(a))
+    assert not np.array_equal(g1["q_fp8"], g2["q_fp8"])
+
+
+def test_live_token_slice():
+    """num_tokens < buffer rows: only the live tokens are read and written."""
+    inp = synth.make_decode(seed=11, T=64, H=8)
+    d = to_device(inp)
+    q_out = torch.full((64, 8, 128), 0x5A, dtype=torch.uint8, device="cuda")
+    w_out = torch.full((64, 8), -7.0, dtype=torch.float32, device="cuda")
+    cache = new_cache(inp)
+    import prep_token_gb300 as dp
+    dp.dsa_indexer_qk_prepare_store(
+        d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
+        d["beta"], inp.eps, inp.softmax_scale, cache, inp.page_size, inp.rope_dim, inp.style,
+        q_fp8_out=q_out.view(torch.float8_e4m3fn), weights_out=w_out, num_tokens=40,
+        max_position=inp.max_position)
+    torch.cuda.synchronize()
+    ref = run_oracle_qk(inp, T=40)
+    got = dict(q_fp8=q_out[:40].cpu().numpy(), weights=w_out[:40].cpu().numpy(),
+               cache=cache.cpu().numpy())
+    inp40 = synth.make_decode(seed=11, T=64, H=8)
+    inp40.T = 40
+    assert_parity(inp40, got, ref)
+    assert torch.all(q_out[40:] == 0x5A) and torch.all(w_out[40:] == -7.0)
+
+
+def test_device_error_bits():
+    inp = synth.make_decode(seed=12, T=20, H=4)
+    inp.positions = inp.positions.copy()
+    inp.slots = inp.slots.copy()
+    inp.positions[3] = -1
+    inp.positions[5] = inp.max_position
+    inp.slots[7] = inp.num_pages * inp.page_size
+    inp.slots[9] = -5
+    d = to_device(inp)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu = run_qk(inp, d, err=err)
+    ref = run_oracle_qk(inp)
+    assert ref["err"] == 3 and int(err.item()) == 3
+    ok = np.ones(inp.T, bool)
+    ok[[3, 5]] = False
+    # tokens with a bad position write nothing; compare the others
+    rep = compare(inp, dict(q_fp8=gpu["q_fp8"][ok], weights=gpu["weights"][ok],
+                            cache=gpu["cache"]),
+                  dict(q_fp8=ref["q_fp8"][ok], weights=ref["weights"][ok], cache=ref["cache"]))
+    assert rep["ok"], rep
+    err.zero_()
+    run_k(inp, d, err=err)
+    assert int(err.item()) == 3
+    err.zero_()
+    good = synth.make_decode(seed=12, T=20, H=4)
+    run_qk(good, to_device(good), err=err)
+    assert int(err.item()) == 0
+
+
+def test_cuda_graph_replay_matches_eager():
+    inp = synth.make_decode(seed=13, T=64, H=64)
+    d = to_device(inp)
+    eager = run_qk(inp, d)
+    import prep_token_gb300 as dp
+    cache = new_cache(inp)
+    q_out = torch.empty((64, 64, 128), dtype=torch.float8_e4m3fn, device="cuda")
+    w_out = torch.empty((64, 64), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dp.dsa_indexer_qk_prepare_store(   # warm up outside capture
+            d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
+            d["beta"], inp.eps, inp.softmax_scale, cache, inp.page_size, inp.rope_dim,
+            inp.style, q_fp8_out=q_out, weights_out=w_out, max_position=inp.max_position)
+    torch.cuda.current_stream().wait_stream(s)
+    cache.fill_(SENTINEL)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dp.dsa_indexer_qk_prepare_store(
+            d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
+            d["beta"], inp.eps, inp.softmax_scale, cache, inp.page_size, inp.rope_dim,
+            inp.style, q_fp8_out=q_out, weights_out=w_out, max_position=inp.max_position)
+    q_out.view(torch.uint8).zero_()
+    cache.fill_(SENTINEL)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(q_out.view(torch.uint8).cpu().numpy(), eager["q_fp8"])
+    assert np.array_equal(w_out.cpu().numpy(), eager["weights"])
+    assert np.array_equal(cache.cpu().numpy(), eager["cache"])
+    # new inputs copied into the captured buffers are picked up on replay
+    inp2 = synth.make_decode(seed=14, T=64, H=64)
+    d2 = to_device(inp2)
+    d["q"].copy_(d2["q"])
+    d["kw"].copy_(d2["kw"])
+    cache.fill_(SENTINEL)
+    g.replay()
+    torch.cuda.synchronize()
+    inp2.positions, inp2.slots = inp.positions, inp.slots
+    inp2.gamma, inp2.beta = inp.gamma, inp.beta
+    got = dict(q_fp8=q_out.view(torch.uint8).cpu().numpy(), weights=w_out.cpu().numpy(),
+               cache=cache.cpu().numpy())
+    assert_parity(inp2, got, run_oracle_qk(inp2))
+
+
+def test_empty_call_launches_nothing():
+    inp = synth.make_tiny(seed=15)
+    d = to_device(inp)
+    cache = new_cache(inp)
+    import prep_token_gb300 as dp
+    q, w = dp.dsa_indexer_qk_prepare_store(
+        d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
+        d["beta"], inp.eps, inp.softmax_scale, cache, inp.page_size, inp.rope_dim, inp.style,
+        num_tokens=0, max_position=inp.max_position)
+    torch.cuda.synchronize()
+    assert q.shape[0] == 0 and w.shape[0] == 0
+    assert torch.all(cache == SENTINEL)
