@@ -150,7 +150,7 @@ def _dev_inputs(inp, dev):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
     kw = bf16(inp.kw)
-    d = dict(q=bf16(inp.q), kw=kw, k=kw[:, :128], w=kw[:, 128:])
+    d = dict(q=bf16(inp.q), kw=kw, k=kw[:, :128], w=kw[:, 128:128 + inp.H])
     for n, key in (("positions", "positions"), ("slots", "slots"), ("cos", "cos"),
                    ("sin", "sin"), ("gamma", "gamma"), ("beta", "beta")):
         d[key] = torch.from_numpy(getattr(inp, n)).to(dev)

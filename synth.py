@@ -39,9 +39,9 @@ class Inputs:
     """Host buffers of one call.  q/k/w hold bf16 bit patterns (uint16).
 
     ``q`` is [T, H, 128] contiguous; ``k`` and ``w`` are views of ``kw``, a
-    [T, 128 + H] buffer laid out like the fused k/weights projection output
-    (k in columns [0, 128), w in [128, 128 + H)), or separate contiguous
-    buffers when ``kw`` is None.  Strides are in elements."""
+    [T, 128 + H (padded to 8)] buffer laid out like the fused k/weights
+    projection output (k in columns [0, 128), w in [128, 128 + H)), or separate
+    contiguous buffers when ``kw`` is None.  Strides are in elements."""
     name: str
     T: int
     H: int
@@ -91,9 +91,6 @@ class Inputs:
         """The buffer k's row stride refers to (flat start at k[0, 0])."""
         return self.kw if self.kw is not None else self.k
 
-    def w_buffer(self):
-        """The buffer w's row stride refers to, starting at w[0, 0]."""
-        return self.kw[:, D:] if self.kw is not None else self.w
 
 
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -167,10 +164,12 @@ def _assemble(name, rng, ss, T, H, rope_dim, style, page_size, num_pages,
     wb = to_bf16_bits(w32).reshape(T, H)
     kw = None
     if fused_kw:
-        kw = np.empty((T, D + H), np.uint16)
+        # row length padded to 8 elements (16 bytes), as a GEMM output's
+        # leading dimension is; the pad columns hold zeros
+        kw = np.zeros((T, (D + H + 7) // 8 * 8), np.uint16)
         kw[:, :D] = kb
-        kw[:, D:] = wb
-        kb, wb = kw[:, :D], kw[:, D:]
+        kw[:, D:D + H] = wb
+        kb, wb = kw[:, :D], kw[:, D:D + H]
     return Inputs(name=name, T=T, H=H, rope_dim=rope_dim, style=style,
                   page_size=page_size, num_pages=num_pages, max_position=max_position,
                   q=q, k=kb, w=wb, positions=positions.astype(np.int64),

@@ -18,7 +18,7 @@ def to_device(inp, device="cuda"):
     if inp.kw is not None:
         kw = bf16_tensor(inp.kw, device)
         d["kw"] = kw
-        d["k"], d["w"] = kw[:, :128], kw[:, 128:]
+        d["k"], d["w"] = kw[:, :128], kw[:, 128:128 + inp.H]
     else:
         d["k"], d["w"] = bf16_tensor(inp.k, device), bf16_tensor(inp.w, device)
     d["positions"] = torch.from_numpy(inp.positions).to(device)
