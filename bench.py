@@ -160,18 +160,18 @@ def _dev_inputs(inp, dev):
     return d
 
 
-def _call(dp, inp, d, stream, T=None, k_only=False):
+def _call(dp, inp, d, stream, T=None, k_only=False, pdl=False):
     if k_only:
         dp.dsa_indexer_k_prepare_store(
             d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
             inp.eps, d["cache"], inp.page_size, inp.rope_dim, inp.style,
-            max_position=inp.max_position, stream=stream, num_tokens=T)
+            max_position=inp.max_position, stream=stream, num_tokens=T, pdl=pdl)
         return
     dp.dsa_indexer_qk_prepare_store(
         d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
         d["beta"], inp.eps, inp.softmax_scale, d["cache"], inp.page_size, inp.rope_dim,
         inp.style, q_fp8_out=d["q_out"], weights_out=d["w_out"],
-        max_position=inp.max_position, stream=stream, num_tokens=T)
+        max_position=inp.max_position, stream=stream, num_tokens=T, pdl=pdl)
 
 
 def _decode_timings(dp, torch, dev, make, label, reps=30, layers=21, k_only_too=False):
@@ -192,11 +192,11 @@ def _decode_timings(dp, torch, dev, make, label, reps=30, layers=21, k_only_too=
                 _call(dp, inp, d, stream, k_only=k_only)
         stream.synchronize()
         res = {}
-        for n_layers in (layers, 1):
+        for n_layers, pdl in ((layers, False), (layers, True), (1, False)):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for inp, d in sets[:n_layers]:
-                    _call(dp, inp, d, stream, k_only=k_only)
+                    _call(dp, inp, d, stream, k_only=k_only, pdl=pdl)
             times = []
             for _ in range(reps):
                 with torch.cuda.stream(stream):
@@ -208,7 +208,8 @@ def _decode_timings(dp, torch, dev, make, label, reps=30, layers=21, k_only_too=
                     e1.record(stream)
                 stream.synchronize()
                 times.append(e0.elapsed_time(e1) * 1000.0 / n_layers)
-            res[f"graph{n_layers}_us"] = {"median": statistics.median(times), "best": min(times)}
+            key = f"graph{n_layers}{'_pdl' if pdl else ''}_us"
+            res[key] = {"median": statistics.median(times), "best": min(times)}
             del g
         # eager: back-to-back calls through the Python binding
         times = []

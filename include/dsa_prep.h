@@ -44,7 +44,9 @@
  *     contiguous.
  *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  No call synchronises the host, so every call can be
- *     captured into a CUDA graph.  One kernel launch per call.
+ *     captured into a CUDA graph.  One kernel launch per call.  The first call
+ *     on a device raises the kernel's dynamic shared-memory limit there (a
+ *     per-device, once-only setting); make it before capturing a graph.
  *   - Host-side checks: a bad argument returns a status other than DSA_OK and
  *     launches nothing.  T == 0 returns DSA_OK and launches nothing.
  *   - Device-side checks: a position outside [0, max_position) sets bit
@@ -52,7 +54,9 @@
  *     q_fp8 rows, weights or cache slot); a slot outside
  *     [0, num_pages * page_size) sets DSA_DEVERR_SLOT and skips that token's
  *     cache write.  err_flags may be NULL (then nothing is reported).  The
- *     kernel never traps.  The caller clears *err_flags.
+ *     kernel never traps and every internal wait is bounded: a wait that
+ *     gives up (never expected) sets DSA_DEVERR_TIMEOUT.  The caller clears
+ *     *err_flags.
  *   - Slots within one call must be distinct (two tokens writing one slot
  *     race).  Inputs must not overlap outputs.
  *   - Non-finite inputs give unspecified codes and scales.
@@ -78,8 +82,17 @@ typedef enum {
 typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
 
 #define DSA_HEAD_DIM 128
-#define DSA_DEVERR_POSITION 1
-#define DSA_DEVERR_SLOT 2
+
+/* Bits of the device error word. */
+#define DSA_DEVERR_POSITION 1 /* a position outside [0, max_position) */
+#define DSA_DEVERR_SLOT 2     /* a slot outside [0, num_pages * page_size) */
+#define DSA_DEVERR_TIMEOUT 4  /* an internal wait gave up (never expected) */
+
+/* Launch flags. */
+#define DSA_FLAG_PDL 1u /* programmatic dependent launch: the kernel may start
+                           while the previous kernel in the stream finishes; it
+                           waits for that kernel's memory before reading
+                           anything */
 
 /*
  * Fused Q/K prepare-and-store: returns the (q_fp8, weights) contract and
@@ -106,7 +119,7 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
  *   index_k_cache  num_pages * page_size * 132 bytes, 16-byte aligned;
  *                  page_size a multiple of 4.
  *   T >= 0, 1 <= H <= 4096, head_dim == 128, rope_dim in {0, 16, ..., 128},
- *   rope_style a dsa_rope_style.
+ *   rope_style a dsa_rope_style, flags a set of DSA_FLAG_* bits.
  */
 dsa_status dsa_indexer_qk_prepare_store(
     const void* q, int64_t q_stride_t, int64_t q_stride_h,
@@ -120,7 +133,7 @@ dsa_status dsa_indexer_qk_prepare_store(
     void* q_fp8_out, float* weights_out,
     void* index_k_cache, int64_t num_pages, int32_t page_size,
     int32_t T, int32_t H, int32_t head_dim, int32_t rope_dim,
-    int32_t rope_style, int32_t* err_flags, void* stream);
+    int32_t rope_style, uint32_t flags, int32_t* err_flags, void* stream);
 
 /*
  * k-only prepare-and-store (the decode fast path of sglang PR "[AMD] [GLM5]
@@ -136,7 +149,7 @@ dsa_status dsa_indexer_k_prepare_store(
     const float* ln_gamma, const float* ln_beta, float ln_eps,
     void* index_k_cache, int64_t num_pages, int32_t page_size,
     int32_t T, int32_t head_dim, int32_t rope_dim, int32_t rope_style,
-    int32_t* err_flags, void* stream);
+    uint32_t flags, int32_t* err_flags, void* stream);
 
 /* A static, NUL-terminated description of a status code. */
 const char* dsa_status_string(dsa_status status);

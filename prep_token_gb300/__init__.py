@@ -23,14 +23,16 @@ import torch
 from ._build import LIB_PATH
 
 __all__ = [
-    "DsaError", "NEOX", "GPTJ", "HEAD_DIM", "DEVERR_POSITION", "DEVERR_SLOT",
+    "DsaError", "NEOX", "GPTJ", "HEAD_DIM", "DEVERR_POSITION", "DEVERR_SLOT", "DEVERR_TIMEOUT",
+    "FLAG_PDL",
     "dsa_indexer_qk_prepare_store", "dsa_indexer_k_prepare_store", "dsa_status_string",
     "library", "cache_bytes", "cache_views",
 ]
 
 NEOX, GPTJ = 0, 1
 HEAD_DIM = 128
-DEVERR_POSITION, DEVERR_SLOT = 1, 2
+DEVERR_POSITION, DEVERR_SLOT, DEVERR_TIMEOUT = 1, 2, 4
+FLAG_PDL = 1
 ROW_BYTES = HEAD_DIM + 4  # 128 codes + one fp32 scale per slot
 
 _STATUS = {0: "DSA_OK", 1: "DSA_ERR_NULL", 2: "DSA_ERR_ALIGN", 3: "DSA_ERR_SHAPE",
@@ -56,12 +58,13 @@ def library() -> ctypes.CDLL:
                 "g.build()'); there is no fallback implementation")
         lib = ctypes.CDLL(LIB_PATH)
         P, I64, I32, F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        U32 = ctypes.c_uint32
         lib.dsa_indexer_qk_prepare_store.argtypes = [
             P, I64, I64, P, I64, P, I64, P, P, P, P, I64, I64, P, P, F32, F32, P, P, P, I64, I32,
-            I32, I32, I32, I32, I32, P, P]
+            I32, I32, I32, I32, I32, U32, P, P]
         lib.dsa_indexer_qk_prepare_store.restype = ctypes.c_int
         lib.dsa_indexer_k_prepare_store.argtypes = [
-            P, I64, P, P, P, P, I64, I64, P, P, F32, P, I64, I32, I32, I32, I32, I32, P, P]
+            P, I64, P, P, P, P, I64, I64, P, P, F32, P, I64, I32, I32, I32, I32, I32, U32, P, P]
         lib.dsa_indexer_k_prepare_store.restype = ctypes.c_int
         lib.dsa_status_string.argtypes = [ctypes.c_int]
         lib.dsa_status_string.restype = ctypes.c_char_p
@@ -146,7 +149,7 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
                                  ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
                                  page_size, rope_dim=64, rope_style=NEOX, *, q_fp8_out=None,
                                  weights_out=None, err_flags=None, num_tokens=None,
-                                 max_position=None, stream=None):
+                                 max_position=None, pdl=False, stream=None):
     """Fused Q/K prepare-and-store (one kernel launch).
 
     q [T, H, 128] bf16, k [T, 128] bf16, w [T, H] bf16 (row strides of any
@@ -154,8 +157,10 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
     [max_position, >= rope_dim/2] fp32, ln_gamma/ln_beta [128] fp32,
     index_k_cache: a contiguous CUDA buffer of whole pages (written in place).
     ``num_tokens`` limits the call to the first T live tokens (the graph
-    split-op contract); outputs are sized to it.  Returns (q_fp8 [T, H, 128]
-    float8_e4m3fn, weights [T, H] fp32)."""
+    split-op contract); outputs are sized to it.  ``pdl`` launches with
+    programmatic dependent launch (the kernel may start while the previous
+    kernel of the stream drains; it still waits for that kernel's memory).
+    Returns (q_fp8 [T, H, 128] float8_e4m3fn, weights [T, H] fp32)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(w, "w", torch.bfloat16, 2)
     cs_stride, rows = _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
@@ -186,7 +191,7 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
         _ptr(sin_cache) if rope_dim else None, cs_stride, max_position, _ptr(ln_gamma),
         _ptr(ln_beta), float(ln_eps), float(softmax_scale), _ptr(q_fp8_out), _ptr(weights_out),
         _ptr(index_k_cache), _num_pages(index_k_cache, page_size), page_size, T, H, HEAD_DIM,
-        rope_dim, int(rope_style), _ptr(err_flags), _stream(stream))
+        rope_dim, int(rope_style), FLAG_PDL if pdl else 0, _ptr(err_flags), _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store")
     return q_fp8_out[:T] if q_fp8_out.dim() == 3 else q_fp8_out, \
@@ -196,7 +201,7 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
 def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
                                 ln_beta, ln_eps, index_k_cache, page_size, rope_dim=64,
                                 rope_style=NEOX, *, err_flags=None, num_tokens=None,
-                                max_position=None, stream=None):
+                                max_position=None, pdl=False, stream=None):
     """k-only prepare-and-store (one kernel launch); writes the cache in place."""
     cs_stride, rows = _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
                                 ln_beta, index_k_cache, rope_dim)
@@ -212,6 +217,6 @@ def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cach
         _ptr(cos_cache) if rope_dim else None, _ptr(sin_cache) if rope_dim else None,
         cs_stride, max_position, _ptr(ln_gamma), _ptr(ln_beta), float(ln_eps),
         _ptr(index_k_cache), _num_pages(index_k_cache, page_size), page_size, T, HEAD_DIM,
-        rope_dim, int(rope_style), _ptr(err_flags), _stream(stream))
+        rope_dim, int(rope_style), FLAG_PDL if pdl else 0, _ptr(err_flags), _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_k_prepare_store")

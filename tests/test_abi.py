@@ -40,7 +40,7 @@ def test_exports_every_declared_symbol(lib):
 def test_status_strings(lib):
     for s in range(6):
         assert dp.dsa_status_string(s)
-    assert lib.dsa_prep_version() >> 16 == 1
+    assert lib.dsa_prep_version() >> 16 == 2
 
 
 A = 0x10000  # a 16-byte aligned fake address: only used by calls that must fail validation
@@ -49,14 +49,14 @@ A = 0x10000  # a 16-byte aligned fake address: only used by calls that must fail
 def _qk(lib, **over):
     args = dict(q=A, sqt=64 * 128, sqh=128, k=A, skt=128, w=A, swt=64, pos=A, loc=A, cos=A,
                 sin=A, cs=32, maxpos=4096, g=A, b=A, eps=1e-6, sm=0.088, qo=A, wo=A, cache=A,
-                pages=4, ps=64, T=4, H=64, D=128, r=64, style=0, err=None, stream=None)
+                pages=4, ps=64, T=4, H=64, D=128, r=64, style=0, flags=0, err=None, stream=None)
     args.update(over)
     return lib.dsa_indexer_qk_prepare_store(*args.values())
 
 
 def _k(lib, **over):
     args = dict(k=A, skt=128, pos=A, loc=A, cos=A, sin=A, cs=32, maxpos=4096, g=A, b=A,
-                eps=1e-6, cache=A, pages=4, ps=64, T=4, D=128, r=64, style=0, err=None,
+                eps=1e-6, cache=A, pages=4, ps=64, T=4, D=128, r=64, style=0, flags=0, err=None,
                 stream=None)
     args.update(over)
     return lib.dsa_indexer_k_prepare_store(*args.values())
@@ -68,7 +68,7 @@ def _k(lib, **over):
     (dict(k=None), 1), (dict(pos=None), 1), (dict(cache=None), 1), (dict(cos=None), 1),
     (dict(ps=6), 2), (dict(k=A + 8), 2), (dict(skt=132), 2), (dict(pos=A + 4), 2),
     (dict(g=A + 4), 2), (dict(cache=A + 8), 2), (dict(cos=A + 4), 2), (dict(cs=34), 2),
-    (dict(cs=16), 3), (dict(skt=-128), 3),
+    (dict(cs=16), 3), (dict(skt=-128), 3), (dict(flags=2), 4), (dict(flags=0x80000000), 4),
 ])
 def test_k_side_validation(lib, over, status):
     assert _k(lib, **over) == status

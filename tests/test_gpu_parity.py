@@ -229,3 +229,54 @@ def test_empty_call_launches_nothing():
     torch.cuda.synchronize()
     assert q.shape[0] == 0 and w.shape[0] == 0
     assert torch.all(cache == SENTINEL)
+
+
+def test_pdl_launch_matches():
+    """Programmatic dependent launch changes when the kernel may start, not
+    what it computes: eager and graph-captured PDL calls give the plain bytes."""
+    inp = synth.make_decode(seed=16, T=64, H=64)
+    d = to_device(inp)
+    plain = run_qk(inp, d)
+    pdl = run_qk(inp, d, pdl=True)
+    for key in ("q_fp8", "weights", "cache"):
+        assert np.array_equal(plain[key], pdl[key]), key
+    import prep_token_gb300 as dp
+    cache = new_cache(inp)
+    q_out = torch.empty((64, 64, 128), dtype=torch.float8_e4m3fn, device="cuda")
+    w_out = torch.empty((64, 64), dtype=torch.float32, device="cuda")
+    k_cache = new_cache(inp)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):   # back-to-back dependent launches inside the graph
+            dp.dsa_indexer_qk_prepare_store(
+                d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"],
+                d["gamma"], d["beta"], inp.eps, inp.softmax_scale, cache, inp.page_size,
+                inp.rope_dim, inp.style, q_fp8_out=q_out, weights_out=w_out,
+                max_position=inp.max_position, pdl=True, stream=s)
+            dp.dsa_indexer_k_prepare_store(
+                d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
+                inp.eps, k_cache, inp.page_size, inp.rope_dim, inp.style,
+                max_position=inp.max_position, pdl=True, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(q_out.view(torch.uint8).cpu().numpy(), plain["q_fp8"])
+    assert np.array_equal(w_out.cpu().numpy(), plain["weights"])
+    assert np.array_equal(cache.cpu().numpy(), plain["cache"])
+    assert np.array_equal(k_cache.cpu().numpy(), plain["cache"])
+
+
+def test_head_stride_not_contiguous_uses_per_head_copies():
+    """q rows that are not packed head after head (sq_h != 128) take one copy
+    per head; the bytes must not change."""
+    b = synth.make_decode(seed=17, T=300, H=24, style=synth.NEOX)
+    db = to_device(b)
+    ref = run_qk(b, db)
+    qpad = torch.zeros((300, 24, 136), dtype=torch.bfloat16, device="cuda")
+    qpad[:, :, :128] = db["q"]
+    dc = dict(db)
+    dc["q"] = qpad[:, :, :128]
+    got = run_qk(b, dc)
+    for key in ("q_fp8", "weights", "cache"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert_parity(b, got, run_oracle_qk(b))
