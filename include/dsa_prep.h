@@ -75,7 +75,7 @@ typedef enum {
   DSA_ERR_NULL = 1,        /* a required pointer is NULL */
   DSA_ERR_ALIGN = 2,       /* a pointer or stride breaks an alignment rule */
   DSA_ERR_SHAPE = 3,       /* a negative or inconsistent size or stride */
-  DSA_ERR_UNSUPPORTED = 4, /* head_dim != 128, bad rope_dim or style, ... */
+  DSA_ERR_UNSUPPORTED = 4, /* head_dim != 128, bad rope_dim, style or flag */
   DSA_ERR_LAUNCH = 5       /* the CUDA launch itself failed */
 } dsa_status;
 
@@ -93,6 +93,13 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
                            while the previous kernel in the stream finishes; it
                            waits for that kernel's memory before reading
                            anything */
+/* Kernel choice.  By default calls with T * H <= 16384 query vectors take the
+ * direct kernel (loads straight to registers: least latency, for decode) and
+ * larger ones the pipeline kernel (bulk copies through a shared-memory ring:
+ * most bandwidth, for prefill).  These flags force one; both give the same
+ * bytes.  Setting both is an error. */
+#define DSA_FLAG_PIPELINE 2u
+#define DSA_FLAG_DIRECT 4u
 
 /*
  * Fused Q/K prepare-and-store: returns the (q_fp8, weights) contract and
@@ -118,7 +125,7 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
  *   weights_out    fp32 [T, H], contiguous, 4-byte aligned.
  *   index_k_cache  num_pages * page_size * 132 bytes, 16-byte aligned;
  *                  page_size a multiple of 4.
- *   T >= 0, 1 <= H <= 4096, head_dim == 128, rope_dim in {0, 16, ..., 128},
+ *   T >= 0, 1 <= H <= 4096, head_dim == 128, rope_dim in {0, 16, 32, 64, 128},
  *   rope_style a dsa_rope_style, flags a set of DSA_FLAG_* bits.
  */
 dsa_status dsa_indexer_qk_prepare_store(

@@ -24,7 +24,7 @@ from ._build import LIB_PATH
 
 __all__ = [
     "DsaError", "NEOX", "GPTJ", "HEAD_DIM", "DEVERR_POSITION", "DEVERR_SLOT", "DEVERR_TIMEOUT",
-    "FLAG_PDL",
+    "FLAG_PDL", "FLAG_PIPELINE", "FLAG_DIRECT",
     "dsa_indexer_qk_prepare_store", "dsa_indexer_k_prepare_store", "dsa_status_string",
     "library", "cache_bytes", "cache_views",
 ]
@@ -32,7 +32,8 @@ __all__ = [
 NEOX, GPTJ = 0, 1
 HEAD_DIM = 128
 DEVERR_POSITION, DEVERR_SLOT, DEVERR_TIMEOUT = 1, 2, 4
-FLAG_PDL = 1
+FLAG_PDL, FLAG_PIPELINE, FLAG_DIRECT = 1, 2, 4
+_KERNEL_FLAGS = {"auto": 0, "pipeline": FLAG_PIPELINE, "direct": FLAG_DIRECT}
 ROW_BYTES = HEAD_DIM + 4  # 128 codes + one fp32 scale per slot
 
 _STATUS = {0: "DSA_OK", 1: "DSA_ERR_NULL", 2: "DSA_ERR_ALIGN", 3: "DSA_ERR_SHAPE",
@@ -119,6 +120,12 @@ def _num_pages(index_k_cache: torch.Tensor, page_size: int) -> int:
     return nbytes // (page_size * ROW_BYTES)
 
 
+def _flags(pdl: bool, kernel: str) -> int:
+    if kernel not in _KERNEL_FLAGS:
+        raise ValueError(f"kernel must be one of {sorted(_KERNEL_FLAGS)}")
+    return (FLAG_PDL if pdl else 0) | _KERNEL_FLAGS[kernel]
+
+
 def _stream(stream) -> int:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -149,7 +156,7 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
                                  ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
                                  page_size, rope_dim=64, rope_style=NEOX, *, q_fp8_out=None,
                                  weights_out=None, err_flags=None, num_tokens=None,
-                                 max_position=None, pdl=False, stream=None):
+                                 max_position=None, pdl=False, kernel="auto", stream=None):
     """Fused Q/K prepare-and-store (one kernel launch).
 
     q [T, H, 128] bf16, k [T, 128] bf16, w [T, H] bf16 (row strides of any
@@ -160,6 +167,8 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
     split-op contract); outputs are sized to it.  ``pdl`` launches with
     programmatic dependent launch (the kernel may start while the previous
     kernel of the stream drains; it still waits for that kernel's memory).
+    ``kernel`` = "auto" | "direct" | "pipeline" overrides the size-based
+    choice between the two kernels (same bytes either way).
     Returns (q_fp8 [T, H, 128] float8_e4m3fn, weights [T, H] fp32)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(w, "w", torch.bfloat16, 2)
@@ -191,7 +200,7 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
         _ptr(sin_cache) if rope_dim else None, cs_stride, max_position, _ptr(ln_gamma),
         _ptr(ln_beta), float(ln_eps), float(softmax_scale), _ptr(q_fp8_out), _ptr(weights_out),
         _ptr(index_k_cache), _num_pages(index_k_cache, page_size), page_size, T, H, HEAD_DIM,
-        rope_dim, int(rope_style), FLAG_PDL if pdl else 0, _ptr(err_flags), _stream(stream))
+        rope_dim, int(rope_style), _flags(pdl, kernel), _ptr(err_flags), _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store")
     return q_fp8_out[:T] if q_fp8_out.dim() == 3 else q_fp8_out, \
@@ -201,7 +210,7 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
 def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
                                 ln_beta, ln_eps, index_k_cache, page_size, rope_dim=64,
                                 rope_style=NEOX, *, err_flags=None, num_tokens=None,
-                                max_position=None, pdl=False, stream=None):
+                                max_position=None, pdl=False, kernel="auto", stream=None):
     """k-only prepare-and-store (one kernel launch); writes the cache in place."""
     cs_stride, rows = _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
                                 ln_beta, index_k_cache, rope_dim)
@@ -217,6 +226,6 @@ def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cach
         _ptr(cos_cache) if rope_dim else None, _ptr(sin_cache) if rope_dim else None,
         cs_stride, max_position, _ptr(ln_gamma), _ptr(ln_beta), float(ln_eps),
         _ptr(index_k_cache), _num_pages(index_k_cache, page_size), page_size, T, HEAD_DIM,
-        rope_dim, int(rope_style), FLAG_PDL if pdl else 0, _ptr(err_flags), _stream(stream))
+        rope_dim, int(rope_style), _flags(pdl, kernel), _ptr(err_flags), _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_k_prepare_store")

@@ -12,7 +12,7 @@ LIB_PATH = os.path.join(PKG, "libdsaprep.so")
 INCLUDE = os.path.join(ROOT, "include")
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
-    "-O3", "-lineinfo", "-std=c++17",
+    "-O3", "-lineinfo", "-std=c++17", "--diag-suppress=177",
     "-Xcompiler", "-fPIC", "-shared",
     "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64",
 ]

@@ -1,4 +1,4 @@
-// DSA indexer Q/K prepare-and-store for GB300 (sm_103a): kernel, launcher
+// DSA indexer Q/K prepare-and-store for GB300 (sm_103a): kernels, launcher
 // and the C ABI declared in include/dsa_prep.h.
 //
 // The work is one streaming pass (HBM-bound, ~1 flop per byte): per token,
@@ -10,26 +10,28 @@
 // fused indexer-Q RoPE+quant kernel for DeepSeek/GLM sparse attention",
 // Summary.)
 //
-// Kernel shape (persistent, warp-specialised):
-//   * a unit of work is one token and a chunk of HC <= 64 of its heads (the
-//     chunk starting at head 0 also carries the token's key);
-//   * warp 0 is the producer: its lane 0 moves each unit's bytes -- the HC
-//     query rows, the key row, the cos/sin rows of the token's position and the
-//     gate weights -- from HBM into a 4-stage shared-memory ring with bulk
-//     asynchronous copies (cp.async.bulk, completion counted on an mbarrier);
-//     the other lanes prefetch positions and slots 32 units ahead;
-//   * warps 1..NCW are consumers: each reads a stage, runs RoPE (+ LayerNorm
-//     for the key), the amax / ue8m0 / e4m3 quantisation and the gate fold in
-//     registers, stores the results straight to global memory, and releases
-//     the stage on its "empty" mbarrier.
-// Bytes in flight are set by the ring depth (up to ~200 KB per SM), not by
-// registers or occupancy.  Every mbarrier wait is bounded in time; on expiry
-// the CTA raises DSA_DEVERR_TIMEOUT, drains its own copies (bounded too) and
-// exits, so a fault can never hang the device.
+// Lane layout ("balanced slices").  A quarter-warp (8 lanes) owns one
+// 128-vector; lane l holds 16 of its elements chosen so that every RoPE pair
+// sits inside one lane and every lane rotates the same number of pairs.  With
+// RP = rope_dim / 16 pairs per lane:
+//   NeoX   a-members  RP elements at  RP*l           (pair partner i + r/2)
+//          b-members  RP elements at  r/2 + RP*l
+//   GPT-J  pairs      2*RP elements at 2*RP*l        (pairs (2i, 2i+1))
+//   both   pass-through 16 - 2*RP elements at r + (16 - 2*RP)*l
+// so the lane's frequencies are RP*l .. RP*l + RP - 1 in both styles, RoPE
+// needs no shuffles, and it runs as packed f32x2 FMUL2/FFMA2.  A warp
+// handles four vectors per instruction stream.
 //
-// Lane layout inside a consumer: a half-warp owns one 128-vector, lane l16
-// holds elements 8*l16 .. 8*l16+7 (one 16-byte shared-memory load, one 8-byte
-// global store of codes).
+// Two kernels share that math:
+//   * dsa_pipeline_kernel (large calls): persistent, warp-specialised.  Warp 0
+//     moves each unit -- one token and up to 64 of its heads, plus the key on
+//     the first chunk -- from HBM into a 4-stage shared-memory ring with
+//     cp.async.bulk copies counted on mbarriers; 8 consumer warps compute from
+//     shared memory and store to HBM.  Bytes in flight are set by the ring
+//     (up to ~200 KB per SM), not by registers.
+//   * dsa_direct_kernel (small calls, decode): one warp per four vectors,
+//     loads straight to registers; the least latency per call.
+// Every mbarrier wait is bounded in time (DSA_DEVERR_TIMEOUT); nothing traps.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -41,27 +43,9 @@
 namespace {
 
 constexpr int kD = DSA_HEAD_DIM;
-constexpr int kHCMax = 64;        // heads per unit at most
-constexpr int kStages = 4;        // shared-memory ring depth
-constexpr int kConsumers = 8;     // consumer warps per CTA
-constexpr int kThreads = 32 * (1 + kConsumers);
 constexpr unsigned kFull = 0xffffffffu;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
-// stage layout (byte offsets from the stage base)
-constexpr int kOffHdr = 0;     // StageHeader
-constexpr int kOffK = 64;      // key row, 256 B
-constexpr int kOffCos = 320;   // cos row, rope_dim/2 floats (<= 256 B)
-constexpr int kOffSin = 576;   // sin row
-constexpr int kOffW = 832;     // gate weights of the chunk, HC bf16 (<= 128 B)
-constexpr int kOffQ = 1024;    // HC query rows of 256 B
-constexpr int kBarrierBytes = 128;  // full[kStages], empty[kStages], abort flag
-
-struct StageHeader {
-  long long pos;
-  long long slot;
-  int pos_ok;
-};
+// ---------------------------------------------------------------- parameters
 
 struct Params {
   const uint16_t* q;
@@ -89,12 +73,17 @@ struct Params {
   int T;
   int H;
   int rope_dim;
-  int cs_bytes;   // rope_dim / 2 * 4
+  int cs_bytes;  // rope_dim / 2 * 4
+  // pipeline kernel
   int HC;         // heads per unit
   int NC;         // units per token
   long long units;
   int stage_bytes;
   int w_bulk;     // the chunk's weights can be bulk-copied (16-byte aligned)
+  // direct kernel
+  int NQ;            // quads of heads per token
+  long long q_warps;  // warps doing q quads
+  long long k_warps;  // warps doing keys (four per warp)
   int* err;
 };
 
@@ -108,6 +97,11 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
                ::"r"(bar), "r"(bytes) : "memory");
@@ -117,13 +111,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One bounded probe: the thread may sleep up to ~1 ms inside it, waking as soon
+// as the phase completes, so waiting warps do not spin on issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+      : "=r"(ok) : "r"(bar), "r"(parity), "r"(1000000) : "memory");
   return ok != 0;
 }
 
@@ -133,18 +129,23 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
 // Wait for the phase with the given parity to complete.  Returns false when
 // the CTA was told to abort or after kWaitLimitNs.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                            volatile int* abort_flag) {
   const unsigned long long t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31) == 0) {
-      if (*abort_flag) return false;
-      if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag);
 }
 
 // Global -> shared bulk copy; completion is counted in bytes on `bar`.
@@ -163,136 +164,278 @@ __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__device__ __forceinline__ uint4 ld_shared16(uint32_t addr) {
-  uint4 r;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
-  return r;
-}
-
-__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
-  float4 r;
-  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(addr));
-  return r;
-}
-
-__device__ __forceinline__ void st_stream8(void* p, uint2 v) {
-  asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
-}
-
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
-__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
-  return __uint_as_float(static_cast<uint32_t>(b) << 16);
-}
-
-__device__ __forceinline__ void unpack_bf16x8(uint4 r, float (&x)[8]) {
-  x[0] = __uint_as_float(r.x << 16);
-  x[1] = __uint_as_float(r.x & 0xffff0000u);
-  x[2] = __uint_as_float(r.y << 16);
-  x[3] = __uint_as_float(r.y & 0xffff0000u);
-  x[4] = __uint_as_float(r.z << 16);
-  x[5] = __uint_as_float(r.z & 0xffff0000u);
-  x[6] = __uint_as_float(r.w << 16);
-  x[7] = __uint_as_float(r.w & 0xffff0000u);
-}
-
 __device__ __forceinline__ float pow2f(int e) {
   return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
-// ---------------------------------------------------------------- the math
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Per-unit rotation operands of this lane.
-//   NeoX: lanes [0, r/16) hold the first members a of pairs 8*l16 .. 8*l16+7,
-//         lanes [r/16, r/8) the second members b of the same pairs.  Every lane
-//         computes own' = fma(own, c, partner * s'), with s' = -s for the
-//         first members (so partner * s' = -(b*s) exactly) and s' = s for the
-//         second ones -- the fused forms a' = fma(a, c, -(b*s)) and
-//         b' = fma(b, c, a*s) with the products rounded to fp32.
-//   GPT-J: lane l16 < r/8 holds pairs 4*l16 .. 4*l16+3 inside its 8 values.
-struct Rot {
-  float c[8];
-  float s[8];
-  bool rot;
-  bool first;
-  int partner;
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// ---------------------------------------------------------------- memory spaces
+
+// Loads of 2/4/8/16 bytes at a byte address, from global (read-only path,
+// streaming) or from shared memory.
+struct GlobalMem {
+  using Addr = const unsigned char*;
+  __device__ __forceinline__ static uint4 ld16(Addr a) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(a));
+    return r;
+  }
+  __device__ __forceinline__ static uint2 ld8(Addr a) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(a));
+    return r;
+  }
+  __device__ __forceinline__ static uint32_t ld4(Addr a) {
+    uint32_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(a));
+    return r;
+  }
+  __device__ __forceinline__ static uint32_t ld2(Addr a) {
+    uint16_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(a));
+    return r;
+  }
 };
 
-template <int STYLE>
-__device__ __forceinline__ void load_rot(Rot& R, uint32_t st, int l16, int rope_dim) {
-  const int rl = rope_dim >> 4;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) R.c[j] = 1.0f, R.s[j] = 0.0f;
-  R.rot = l16 < 2 * rl;
-  R.first = l16 < rl;
-  R.partner = R.first ? l16 + rl : (R.rot ? l16 - rl : l16);
-  if (!R.rot) return;
-  if (STYLE == DSA_ROPE_NEOX) {
-    const int base = 4 * 8 * (R.first ? l16 : l16 - rl);
-    const float4 c0 = ld_shared_f4(st + kOffCos + base), c1 = ld_shared_f4(st + kOffCos + base + 16);
-    const float4 s0 = ld_shared_f4(st + kOffSin + base), s1 = ld_shared_f4(st + kOffSin + base + 16);
-    R.c[0] = c0.x; R.c[1] = c0.y; R.c[2] = c0.z; R.c[3] = c0.w;
-    R.c[4] = c1.x; R.c[5] = c1.y; R.c[6] = c1.z; R.c[7] = c1.w;
-    R.s[0] = s0.x; R.s[1] = s0.y; R.s[2] = s0.z; R.s[3] = s0.w;
-    R.s[4] = s1.x; R.s[5] = s1.y; R.s[6] = s1.z; R.s[7] = s1.w;
-    if (R.first) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) R.s[j] = -R.s[j];
-    }
-  } else {
-    const float4 c0 = ld_shared_f4(st + kOffCos + 16 * l16);
-    const float4 s0 = ld_shared_f4(st + kOffSin + 16 * l16);
-    R.c[0] = c0.x; R.c[1] = c0.y; R.c[2] = c0.z; R.c[3] = c0.w;
-    R.s[0] = s0.x; R.s[1] = s0.y; R.s[2] = s0.z; R.s[3] = s0.w;
+struct SharedMem {
+  using Addr = uint32_t;
+  __device__ __forceinline__ static uint4 ld16(Addr a) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
+    return r;
   }
-}
+  __device__ __forceinline__ static uint2 ld8(Addr a) {
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
+    return r;
+  }
+  __device__ __forceinline__ static uint32_t ld4(Addr a) {
+    uint32_t r;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(a));
+    return r;
+  }
+  __device__ __forceinline__ static uint32_t ld2(Addr a) {
+    uint16_t r;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(r) : "r"(a));
+    return r;
+  }
+};
 
-// RoPE on this lane's 8 values.  Every lane of the warp must call it (NeoX
-// exchanges values with the lane r/16 away).
-template <int STYLE>
-__device__ __forceinline__ void rope_apply(float (&x)[8], const Rot& R) {
-  if (STYLE == DSA_ROPE_NEOX) {
-    float o[8];
+__host__ __device__ constexpr int pow2_floor(int x) { return x >= 16 ? 16 : x >= 8 ? 8 : x >= 4 ? 4 : x >= 2 ? 2 : 1; }
+__host__ __device__ constexpr int gcd_pow2(int x) { return x == 0 ? 16 : (x & -x) > 16 ? 16 : (x & -x); }
+
+// `BYTES` bytes at `a` (aligned to ALIGN) as 32-bit words w[]; 2-byte pieces
+// land in the low half of a word.
+template <class M, int BYTES, int ALIGN>
+__device__ __forceinline__ void load_words(typename M::Addr a, uint32_t* w) {
+  constexpr int W = pow2_floor(ALIGN < BYTES ? ALIGN : BYTES);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) o[j] = __shfl_sync(kFull, x[j], R.partner, 16);
-    if (R.rot) {
-#pragma unroll
-      for (int j = 0; j < 8; j += 2) {
-        const float2 ps = __fmul2_rn(make_float2(o[j], o[j + 1]), make_float2(R.s[j], R.s[j + 1]));
-        const float2 r = __ffma2_rn(make_float2(x[j], x[j + 1]), make_float2(R.c[j], R.c[j + 1]), ps);
-        x[j] = r.x;
-        x[j + 1] = r.y;
-      }
-    }
-  } else {
-    if (R.rot) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float a = x[2 * j], b = x[2 * j + 1];
-        x[2 * j] = __fmaf_rn(a, R.c[j], -__fmul_rn(b, R.s[j]));
-        x[2 * j + 1] = __fmaf_rn(b, R.c[j], __fmul_rn(a, R.s[j]));
-      }
+  for (int b = 0; b < BYTES; b += W) {
+    if constexpr (W == 16) {
+      const uint4 v = M::ld16(a + b);
+      w[b / 4] = v.x; w[b / 4 + 1] = v.y; w[b / 4 + 2] = v.z; w[b / 4 + 3] = v.w;
+    } else if constexpr (W == 8) {
+      const uint2 v = M::ld8(a + b);
+      w[b / 4] = v.x; w[b / 4 + 1] = v.y;
+    } else if constexpr (W == 4) {
+      w[b / 4] = M::ld4(a + b);
+    } else {
+      w[b / 4] = M::ld2(a + b);
     }
   }
 }
 
-// Half-warp reductions (xor offsets 8..1 never leave the 16-lane group).
-__device__ __forceinline__ float halfwarp_max(float v) {
-  v = fmaxf(v, __shfl_xor_sync(kFull, v, 8));
+// N bf16 elements -> fp32 x[0..N)
+template <class M, int N, int ALIGN>
+__device__ __forceinline__ void load_bf16(typename M::Addr a, float* x) {
+  uint32_t w[(2 * N + 3) / 4];
+  load_words<M, 2 * N, ALIGN>(a, w);
+#pragma unroll
+  for (int j = 0; j < N; ++j) x[j] = (j & 1) ? bf16_hi(w[j / 2]) : bf16_lo(w[j / 2]);
+}
+
+// N fp32 values from global (gamma / beta / cos / sin rows), read-only cached.
+template <int N, int ALIGN>
+__device__ __forceinline__ void load_f32_global(const float* p, float* x) {
+  constexpr int W = pow2_floor(ALIGN < 4 * N ? ALIGN : 4 * N);
+#pragma unroll
+  for (int b = 0; b < 4 * N; b += W) {
+    if constexpr (W == 16) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(p + b / 4));
+      x[b / 4] = v.x; x[b / 4 + 1] = v.y; x[b / 4 + 2] = v.z; x[b / 4 + 3] = v.w;
+    } else if constexpr (W == 8) {
+      const float2 v = __ldg(reinterpret_cast<const float2*>(p + b / 4));
+      x[b / 4] = v.x; x[b / 4 + 1] = v.y;
+    } else {
+      x[b / 4] = __ldg(p + b / 4);
+    }
+  }
+}
+
+template <int N, int ALIGN>
+__device__ __forceinline__ void load_f32_shared(uint32_t a, float* x) {
+  uint32_t w[N];
+  load_words<SharedMem, 4 * N, ALIGN>(a, w);
+#pragma unroll
+  for (int j = 0; j < N; ++j) x[j] = __uint_as_float(w[j]);
+}
+
+// Store `BYTES` code bytes (packed little-endian in w[]) at global p.
+template <int BYTES, int ALIGN>
+__device__ __forceinline__ void store_codes(uint8_t* p, const uint32_t* w) {
+  constexpr int W = pow2_floor(ALIGN < BYTES ? ALIGN : BYTES);
+#pragma unroll
+  for (int b = 0; b < BYTES; b += W) {
+    if constexpr (W == 16) {
+      asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p + b), "r"(w[b / 4]),
+                   "r"(w[b / 4 + 1]), "r"(w[b / 4 + 2]), "r"(w[b / 4 + 3]) : "memory");
+    } else if constexpr (W == 8) {
+      asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p + b), "r"(w[b / 4]),
+                   "r"(w[b / 4 + 1]) : "memory");
+    } else if constexpr (W == 4) {
+      asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p + b), "r"(w[b / 4]) : "memory");
+    } else if constexpr (W == 2) {
+      const uint16_t v = static_cast<uint16_t>(w[b / 4] >> (8 * (b & 3)));
+      asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p + b), "h"(v) : "memory");
+    } else {
+      const uint16_t v = static_cast<uint16_t>((w[b / 4] >> (8 * (b & 3))) & 0xff);
+      asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p + b), "h"(v) : "memory");
+    }
+  }
+}
+
+// ---------------------------------------------------------------- the slice
+
+// Where a lane's 16 elements live (element offsets inside the 128-vector and
+// their alignment in bytes for bf16 / e4m3 / fp32 rows).
+template <int STYLE, int RP>
+struct Slice {
+  static constexpr int R = 16 * RP;      // rope_dim
+  static constexpr int NR = 2 * RP;      // rotated elements per lane
+  static constexpr int NP = 16 - NR;     // pass-through elements per lane
+  static constexpr bool NEOX = STYLE == DSA_ROPE_NEOX;
+  // element offset of each chunk for lane l: base + stride * l
+  static constexpr int A_STRIDE = NEOX ? RP : 2 * RP;  // NeoX a-chunk / GPT-J pair chunk
+  static constexpr int B_BASE = R / 2;                  // NeoX b-chunk
+  static constexpr int P_BASE = R;
+  // alignments (bytes) of the per-lane chunk starts
+  static constexpr int ALIGN_A_BF16 = gcd_pow2(2 * A_STRIDE);
+  static constexpr int ALIGN_B_BF16 = gcd_pow2(2 * RP) < gcd_pow2(2 * B_BASE) ? gcd_pow2(2 * RP)
+                                                                               : gcd_pow2(2 * B_BASE);
+  static constexpr int ALIGN_P_BF16 = gcd_pow2(2 * NP) < gcd_pow2(2 * P_BASE) ? gcd_pow2(2 * NP)
+                                                                               : gcd_pow2(2 * P_BASE);
+  static constexpr int ALIGN_A_U8 = gcd_pow2(A_STRIDE);
+  static constexpr int ALIGN_B_U8 = gcd_pow2(RP) < gcd_pow2(B_BASE) ? gcd_pow2(RP) : gcd_pow2(B_BASE);
+  static constexpr int ALIGN_P_U8 = gcd_pow2(NP) < gcd_pow2(P_BASE) ? gcd_pow2(NP) : gcd_pow2(P_BASE);
+  static constexpr int ALIGN_A_F32 = gcd_pow2(4 * A_STRIDE);
+  static constexpr int ALIGN_B_F32 = gcd_pow2(4 * RP) < gcd_pow2(4 * B_BASE) ? gcd_pow2(4 * RP)
+                                                                               : gcd_pow2(4 * B_BASE);
+  static constexpr int ALIGN_P_F32 = gcd_pow2(4 * NP) < gcd_pow2(4 * P_BASE) ? gcd_pow2(4 * NP)
+                                                                               : gcd_pow2(4 * P_BASE);
+  static constexpr int ALIGN_CS = gcd_pow2(4 * RP);
+};
+
+// Load the lane's 16 bf16 values of a row into x[]: x[0..RP) the a-members,
+// x[RP..2RP) the b-members, x[2RP..16) the pass-through values.
+template <int STYLE, int RP, class M>
+__device__ __forceinline__ void load_slice(typename M::Addr row, int l, float (&x)[16]) {
+  using S = Slice<STYLE, RP>;
+  if constexpr (RP > 0) {
+    if constexpr (S::NEOX) {
+      load_bf16<M, RP, S::ALIGN_A_BF16>(row + 2 * RP * l, x);
+      load_bf16<M, RP, S::ALIGN_B_BF16>(row + 2 * (S::B_BASE + RP * l), x + RP);
+    } else {
+      float t[2 * RP];
+      load_bf16<M, 2 * RP, S::ALIGN_A_BF16>(row + 4 * RP * l, t);
+#pragma unroll
+      for (int j = 0; j < RP; ++j) x[j] = t[2 * j], x[RP + j] = t[2 * j + 1];
+    }
+  }
+  if constexpr (S::NP > 0) load_bf16<M, S::NP, S::ALIGN_P_BF16>(row + 2 * (S::P_BASE + S::NP * l), x + 2 * RP);
+}
+
+// The same slice of an fp32 row (LayerNorm gamma / beta).
+template <int STYLE, int RP>
+__device__ __forceinline__ void load_slice_f32(const float* row, int l, float (&x)[16]) {
+  using S = Slice<STYLE, RP>;
+  if constexpr (RP > 0) {
+    if constexpr (S::NEOX) {
+      load_f32_global<RP, S::ALIGN_A_F32>(row + RP * l, x);
+      load_f32_global<RP, S::ALIGN_B_F32>(row + S::B_BASE + RP * l, x + RP);
+    } else {
+      float t[2 * RP];
+      load_f32_global<2 * RP, S::ALIGN_A_F32>(row + 2 * RP * l, t);
+#pragma unroll
+      for (int j = 0; j < RP; ++j) x[j] = t[2 * j], x[RP + j] = t[2 * j + 1];
+    }
+  }
+  if constexpr (S::NP > 0) load_f32_global<S::NP, S::ALIGN_P_F32>(row + S::P_BASE + S::NP * l, x + 2 * RP);
+}
+
+// Rotation operands of the lane: frequencies RP*l .. RP*l + RP - 1.
+template <int RP>
+struct Rot {
+  float c[RP > 0 ? RP : 1];
+  float s[RP > 0 ? RP : 1];
+  float ns[RP > 0 ? RP : 1];
+};
+
+template <int RP>
+__device__ __forceinline__ void finish_rot(Rot<RP>& r) {
+#pragma unroll
+  for (int j = 0; j < RP; ++j) r.ns[j] = -r.s[j];
+}
+
+// RoPE on the lane's pairs (a_j, b_j):
+//   a' = fma(a, c, b * (-s)) = fma(a, c, -(b*s)),  b' = fma(b, c, a * s),
+// products rounded to fp32 (no contraction), two pairs per packed instruction.
+template <int RP>
+__device__ __forceinline__ void rope_slice(float (&x)[16], const Rot<RP>& r) {
+  if constexpr (RP == 1) {
+    const float a = x[0], b = x[1];
+    x[0] = __fmaf_rn(a, r.c[0], __fmul_rn(b, r.ns[0]));
+    x[1] = __fmaf_rn(b, r.c[0], __fmul_rn(a, r.s[0]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < RP; j += 2) {
+      const float2 a = make_float2(x[j], x[j + 1]);
+      const float2 b = make_float2(x[RP + j], x[RP + j + 1]);
+      const float2 c = make_float2(r.c[j], r.c[j + 1]);
+      const float2 pa = __fmul2_rn(b, make_float2(r.ns[j], r.ns[j + 1]));
+      const float2 pb = __fmul2_rn(a, make_float2(r.s[j], r.s[j + 1]));
+      const float2 na = __ffma2_rn(a, c, pa);
+      const float2 nb = __ffma2_rn(b, c, pb);
+      x[j] = na.x; x[j + 1] = na.y;
+      x[RP + j] = nb.x; x[RP + j + 1] = nb.y;
+    }
+  }
+}
+
+// Quarter-warp reductions (xor offsets 4, 2, 1 stay inside the 8-lane group).
+__device__ __forceinline__ float quad_max(float v) {
   v = fmaxf(v, __shfl_xor_sync(kFull, v, 4));
   v = fmaxf(v, __shfl_xor_sync(kFull, v, 2));
   v = fmaxf(v, __shfl_xor_sync(kFull, v, 1));
   return v;
 }
 
-__device__ __forceinline__ float halfwarp_sum(float v) {
-  v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 8));
+__device__ __forceinline__ float quad_sum(float v) {
   v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 4));
   v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 2));
   v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 1));
@@ -303,39 +446,219 @@ __device__ __forceinline__ float halfwarp_sum(float v) {
 // With A = max(amax, 1e-4) = 1.f * 2^E (normal), 448 * 2^e = 1.75 * 2^(e+8), so
 // e = E - 8 when the fraction is <= 0.75 (bits <= 0x600000) and E - 7 above:
 // read straight off the exponent and fraction bits, no division or log.
-__device__ __forceinline__ int ue8m0_exponent(const float (&x)[8]) {
-  float m01, m23;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(m01) : "f"(fabsf(x[0])), "f"(fabsf(x[1])), "f"(fabsf(x[2])));
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(m23) : "f"(fabsf(x[3])), "f"(fabsf(x[4])), "f"(fabsf(x[5])));
-  float m;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(m01), "f"(m23), "f"(fabsf(x[6])));
-  m = fmaxf(m, fabsf(x[7]));
-  m = fmaxf(halfwarp_max(m), 1e-4f);
+__device__ __forceinline__ int ue8m0_exponent(const float (&x)[16]) {
+  float m = max3f(fabsf(x[0]), fabsf(x[1]), fabsf(x[2]));
+#pragma unroll
+  for (int j = 3; j < 15; j += 2) m = max3f(m, fabsf(x[j]), fabsf(x[j + 1]));
+  m = fmaxf(m, fabsf(x[15]));
+  m = fmaxf(quad_max(m), 1e-4f);
   const uint32_t b = __float_as_uint(m);
   return static_cast<int>(b >> 23) - 135 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0);
 }
 
-// codes = e4m3_rne(x * 2^-e): the multiply by a power of two is exact.
-__device__ __forceinline__ uint2 quantize8(const float (&x)[8], int e) {
+// e4m3 codes of x * 2^-e (the multiply by a power of two is exact), packed in
+// element order of each chunk: words wa (a-chunk or GPT-J pair chunk), wb
+// (NeoX b-chunk), wp (pass-through chunk).
+template <int STYLE, int RP>
+__device__ __forceinline__ void quantize_slice(const float (&x)[16], int e, uint32_t* wa,
+                                               uint32_t* wb, uint32_t* wp) {
+  using S = Slice<STYLE, RP>;
   const float inv = pow2f(-e);
   const float2 i2 = make_float2(inv, inv);
-  const float2 v0 = __fmul2_rn(make_float2(x[0], x[1]), i2);
-  const float2 v1 = __fmul2_rn(make_float2(x[2], x[3]), i2);
-  const float2 v2 = __fmul2_rn(make_float2(x[4], x[5]), i2);
-  const float2 v3 = __fmul2_rn(make_float2(x[6], x[7]), i2);
-  const uint32_t p0 = cvt_e4m3x2(v0.x, v0.y), p1 = cvt_e4m3x2(v1.x, v1.y);
-  const uint32_t p2 = cvt_e4m3x2(v2.x, v2.y), p3 = cvt_e4m3x2(v3.x, v3.y);
-  return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const float2 t = __fmul2_rn(make_float2(x[j], x[j + 1]), i2);
+    v[j] = t.x;
+    v[j + 1] = t.y;
+  }
+  if constexpr (RP > 0) {
+    if constexpr (S::NEOX) {
+      // a-chunk: v[0..RP), b-chunk: v[RP..2RP); RP = 1 packs a lone code
+#pragma unroll
+      for (int j = 0; j < RP; j += 2) {
+        const uint32_t ca = cvt_e4m3x2(v[j], RP > 1 ? v[j + 1] : 0.0f);
+        const uint32_t cb = cvt_e4m3x2(v[RP + j], RP > 1 ? v[RP + j + 1] : 0.0f);
+        if ((j & 2) == 0) wa[j / 4] = ca, wb[j / 4] = cb;
+        else wa[j / 4] |= ca << 16, wb[j / 4] |= cb << 16;
+      }
+    } else {
+      // pair chunk in element order: a_0 b_0 a_1 b_1 ...
+#pragma unroll
+      for (int j = 0; j < RP; ++j) {
+        const uint32_t c = cvt_e4m3x2(v[j], v[RP + j]);
+        if ((j & 1) == 0) wa[j / 2] = c;
+        else wa[j / 2] |= c << 16;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < S::NP; j += 2) {
+    const uint32_t c = cvt_e4m3x2(v[2 * RP + j], v[2 * RP + j + 1]);
+    if ((j & 2) == 0) wp[j / 4] = c;
+    else wp[j / 4] |= c << 16;
+  }
 }
 
-// ---------------------------------------------------------------- roles
+template <int STYLE, int RP>
+__device__ __forceinline__ void store_slice(uint8_t* row, int l, const uint32_t* wa,
+                                            const uint32_t* wb, const uint32_t* wp) {
+  using S = Slice<STYLE, RP>;
+  if constexpr (RP > 0) {
+    if constexpr (S::NEOX) {
+      store_codes<RP, S::ALIGN_A_U8>(row + RP * l, wa);
+      store_codes<RP, S::ALIGN_B_U8>(row + S::B_BASE + RP * l, wb);
+    } else {
+      store_codes<2 * RP, S::ALIGN_A_U8>(row + 2 * RP * l, wa);
+    }
+  }
+  if constexpr (S::NP > 0) store_codes<S::NP, S::ALIGN_P_U8>(row + S::P_BASE + S::NP * l, wp);
+}
+
+// Query vector: rotate, quantise, store codes; returns the scale exponent.
+template <int STYLE, int RP>
+__device__ __forceinline__ int q_slice(float (&x)[16], const Rot<RP>& r, uint8_t* out_row,
+                                       int l, bool store) {
+  if constexpr (RP > 0) rope_slice<RP>(x, r);
+  const int e = ue8m0_exponent(x);
+  uint32_t wa[4], wb[4], wp[4];
+  quantize_slice<STYLE, RP>(x, e, wa, wb, wp);
+  if (store) store_slice<STYLE, RP>(out_row, l, wa, wb, wp);
+  return e;
+}
 
 __device__ __forceinline__ void raise_error(const Params& p, int bit) {
   if (p.err) atomicOr(p.err, bit);
 }
 
+// Key vector: LayerNorm (mean, biased variance, eps inside the root), RoPE,
+// quantise, and store the codes and the scale into slot `slot` of the cache.
+template <int STYLE, int RP>
+__device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const Rot<RP>& r,
+                                        int l, bool real, bool pos_ok, long long slot) {
+  float g[16], bt[16];
+  load_slice_f32<STYLE, RP>(p.gamma, l, g);
+  load_slice_f32<STYLE, RP>(p.beta, l, bt);
+  float sum = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) sum = __fadd_rn(sum, x[j]);
+  const float mean = __fmul_rn(quad_sum(sum), 1.0f / kD);
+  float sq = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    x[j] = __fsub_rn(x[j], mean);
+    sq = __fmaf_rn(x[j], x[j], sq);
+  }
+  const float var = __fmul_rn(quad_sum(sq), 1.0f / kD);
+  const float rstd = __frsqrt_rn(__fadd_rn(var, p.eps));
+#pragma unroll
+  for (int j = 0; j < 16; ++j) x[j] = __fmaf_rn(__fmul_rn(x[j], rstd), g[j], bt[j]);
+  if constexpr (RP > 0) rope_slice<RP>(x, r);
+  const int e = ue8m0_exponent(x);
+  uint32_t wa[4], wb[4], wp[4];
+  quantize_slice<STYLE, RP>(x, e, wa, wb, wp);
+
+  if (!real) return;
+  if (!pos_ok) {
+    if (l == 0) raise_error(p, DSA_DEVERR_POSITION);
+    return;
+  }
+  if (slot < 0 || slot >= p.num_slots) {
+    if (l == 0) raise_error(p, DSA_DEVERR_SLOT);
+    return;
+  }
+  const long long page = slot / p.page_size;
+  const long long off = slot - page * p.page_size;
+  uint8_t* base = p.cache + page * p.page_bytes;
+  store_slice<STYLE, RP>(base + off * kD, l, wa, wb, wp);
+  if (l == 0)
+    *reinterpret_cast<float*>(base + static_cast<long long>(p.page_size) * kD + 4 * off) = pow2f(e);
+}
+
+// ================================================================ direct kernel
+
+constexpr int kDirectThreads = 256;
+
+// cos/sin of the lane's frequencies at row `row`, from global memory.
+template <int RP>
+__device__ __forceinline__ void load_rot_global(const Params& p, long long row, int l, Rot<RP>& r) {
+  if constexpr (RP > 0) {
+    load_f32_global<RP, Slice<0, RP>::ALIGN_CS>(p.cos_t + row * p.cs_stride + RP * l, r.c);
+    load_f32_global<RP, Slice<0, RP>::ALIGN_CS>(p.sin_t + row * p.cs_stride + RP * l, r.s);
+    finish_rot<RP>(r);
+  }
+}
+
+template <int STYLE, int RP>
+__global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params p) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int qtr = lane >> 3;
+  const int l = lane & 7;
+  const long long u = static_cast<long long>(blockIdx.x) * (kDirectThreads / 32) + (threadIdx.x >> 5);
+  if (u >= p.q_warps + p.k_warps) return;  // warp-uniform
+
+  if (u < p.q_warps) {
+    // four heads of one token
+    const long long t = u / p.NQ;
+    const int v = static_cast<int>(u - t * p.NQ) * 4 + qtr;
+    const bool valid = v < p.H;
+    const long long pos = __ldg(p.pos + t);
+    float x[16] = {};
+    if (valid) {
+      const unsigned char* row = reinterpret_cast<const unsigned char*>(p.q + t * p.sq_t + v * p.sq_h);
+      load_slice<STYLE, RP, GlobalMem>(row, l, x);
+    }
+    float wv = 0.0f;
+    if (valid && l == 0) wv = __uint_as_float(static_cast<uint32_t>(__ldg(p.w + t * p.sw_t + v)) << 16);
+    const bool pos_ok = pos >= 0 && pos < p.max_pos;
+    Rot<RP> r;
+    load_rot_global<RP>(p, pos_ok ? pos : 0, l, r);
+    const long long orow = t * p.H + v;
+    const int e = q_slice<STYLE, RP>(x, r, p.q_out + orow * kD, l, valid && pos_ok);
+    if (valid && pos_ok && l == 0) __stcs(p.w_out + orow, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold));
+  } else {
+    // four keys, one per quarter-warp
+    const long long t = 4 * (u - p.q_warps) + qtr;
+    const bool real = t < p.T;
+    const long long tt = real ? t : 0;
+    const long long pos = __ldg(p.pos + tt);
+    const long long slot = __ldg(p.loc + tt);
+    float x[16];
+    load_slice<STYLE, RP, GlobalMem>(reinterpret_cast<const unsigned char*>(p.k + tt * p.sk_t), l, x);
+    const bool pos_ok = pos >= 0 && pos < p.max_pos;
+    Rot<RP> r;
+    load_rot_global<RP>(p, pos_ok ? pos : 0, l, r);
+    k_slice<STYLE, RP>(p, x, r, l, real, pos_ok, slot);
+  }
+}
+
+// ================================================================ pipeline kernel
+
+constexpr int kHCMax = 64;        // heads per unit at most
+constexpr int kStages = 4;        // shared-memory ring depth
+constexpr int kConsumers = 8;     // consumer warps per CTA
+constexpr int kPipeThreads = 32 * (1 + kConsumers);
+
+// stage layout (byte offsets from the stage base)
+constexpr int kOffHdr = 0;     // StageHeader
+constexpr int kOffK = 64;      // key row, 256 B
+constexpr int kOffCos = 320;   // cos row, rope_dim/2 floats (<= 256 B)
+constexpr int kOffSin = 576;   // sin row
+constexpr int kOffW = 832;     // gate weights of the chunk, HC bf16 (<= 128 B)
+constexpr int kOffQ = 1024;    // HC query rows of 256 B
+constexpr int kBarrierBytes = 128;  // full[kStages], empty[kStages], abort flag
+
+struct StageHeader {
+  long long pos;
+  long long slot;
+  int pos_ok;
+};
+
 // Producer warp: lane 0 fills the ring; all lanes prefetch (position, slot)
-// for the next 32 units of this CTA.
+// for the next 32 units of this CTA.  The position-independent copies (query
+// rows, key row, weights) go out before the position is known.
 __device__ void producer(const Params& p, unsigned char* ring, uint32_t full0, uint32_t empty0,
                          volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
@@ -353,32 +676,23 @@ __device__ void producer(const Params& p, unsigned char* ring, uint32_t full0, u
         if (uu - tt * p.NC == 0) my_slot = __ldg(p.loc + tt);
       }
     }
-    const long long pos = __shfl_sync(kFull, my_pos, j);
-    const long long slot = __shfl_sync(kFull, my_slot, j);
     int stop = 0;
+    const int s = i % kStages;
+    const uint32_t full = full0 + 8 * s;
+    unsigned char* st = ring + static_cast<size_t>(s) * p.stage_bytes;
+    const uint32_t sts = smem_u32(st);
+    const long long t = u / p.NC;
+    const int c = static_cast<int>(u - t * p.NC);
     if (lane == 0) {
-      const int s = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
-      const uint32_t full = full0 + 8 * s, empty = empty0 + 8 * s;
-      unsigned char* st = ring + static_cast<size_t>(s) * p.stage_bytes;
-      const uint32_t sts = smem_u32(st);
-      if (i >= kStages && !mbar_wait(empty, ph ^ 1, abort_flag)) {
+      if (i >= kStages && !mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag)) {
         stop = 1;
       } else {
-        const long long t = u / p.NC;
-        const int c = static_cast<int>(u - t * p.NC);
         const int h0 = c * p.HC;
         const int n = min(p.HC, p.H - h0);
-        const bool pos_ok = pos >= 0 && pos < p.max_pos;
-        const long long row = pos_ok ? pos : 0;
-        StageHeader* hd = reinterpret_cast<StageHeader*>(st + kOffHdr);
-        hd->pos = pos;
-        hd->slot = slot;
-        hd->pos_ok = pos_ok ? 1 : 0;
-        const uint32_t bytes = static_cast<uint32_t>(n) * 256u + (c == 0 ? 256u : 0u) +
-                               (p.rope_dim ? 2u * p.cs_bytes : 0u) +
+        const uint32_t early = static_cast<uint32_t>(n) * 256u + (c == 0 ? 256u : 0u) +
                                (p.w_bulk ? 2u * n : 0u);
-        mbar_arrive_expect_tx(full, bytes);
+        if (early) mbar_expect_tx(full, early);
         if (n > 0) {
           const uint16_t* qsrc = p.q + t * p.sq_t + static_cast<long long>(h0) * p.sq_h;
           if (p.sq_h == kD) {
@@ -389,10 +703,6 @@ __device__ void producer(const Params& p, unsigned char* ring, uint32_t full0, u
           if (p.w_bulk) bulk_g2s(sts + kOffW, p.w + t * p.sw_t + h0, 2u * n, full);
         }
         if (c == 0) bulk_g2s(sts + kOffK, p.k + t * p.sk_t, 256u, full);
-        if (p.rope_dim) {
-          bulk_g2s(sts + kOffCos, p.cos_t + row * p.cs_stride, p.cs_bytes, full);
-          bulk_g2s(sts + kOffSin, p.sin_t + row * p.cs_stride, p.cs_bytes, full);
-        }
       }
     }
     stop = __shfl_sync(kFull, stop, 0);
@@ -403,6 +713,24 @@ __device__ void producer(const Params& p, unsigned char* ring, uint32_t full0, u
       }
       break;
     }
+    const long long pos = __shfl_sync(kFull, my_pos, j);
+    const long long slot = __shfl_sync(kFull, my_slot, j);
+    if (lane == 0) {
+      const bool pos_ok = pos >= 0 && pos < p.max_pos;
+      const long long row = pos_ok ? pos : 0;
+      StageHeader* hd = reinterpret_cast<StageHeader*>(st + kOffHdr);
+      hd->pos = pos;
+      hd->slot = slot;
+      hd->pos_ok = pos_ok ? 1 : 0;
+      if (p.rope_dim) {
+        mbar_arrive_expect_tx(full, 2u * p.cs_bytes);
+        bulk_g2s(sts + kOffCos, p.cos_t + row * p.cs_stride, p.cs_bytes, full);
+        bulk_g2s(sts + kOffSin, p.sin_t + row * p.cs_stride, p.cs_bytes, full);
+      } else {
+        mbar_arrive(full);
+      }
+    }
+    __syncwarp();
   }
   // Stay until the copies of the last (up to kStages) units have landed, so
   // the CTA never exits with a bulk copy still writing its shared memory.
@@ -413,74 +741,12 @@ __device__ void producer(const Params& p, unsigned char* ring, uint32_t full0, u
   }
 }
 
-// One q vector (half-warp) -> codes, returns the scale exponent.
-template <int STYLE>
-__device__ __forceinline__ int q_vector(uint4 raw, const Rot& R, uint2& codes) {
-  float x[8];
-  unpack_bf16x8(raw, x);
-  rope_apply<STYLE>(x, R);
-  const int e = ue8m0_exponent(x);
-  codes = quantize8(x, e);
-  return e;
-}
-
-// The key of one token (half-warp): LayerNorm, RoPE, quantise, cache store.
-template <int STYLE>
-__device__ __forceinline__ void k_vector(const Params& p, uint32_t sts, const StageHeader& hd,
-                                         const Rot& R, bool real, int l16) {
-  const uint4 raw = ld_shared16(sts + kOffK + 16 * l16);
-  const float4* g4 = reinterpret_cast<const float4*>(p.gamma + 8 * l16);
-  const float4* b4 = reinterpret_cast<const float4*>(p.beta + 8 * l16);
-  const float4 g0 = __ldg(g4), g1 = __ldg(g4 + 1), b0 = __ldg(b4), b1 = __ldg(b4 + 1);
-  const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-  const float bt[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-
-  // LayerNorm: mean, biased variance, eps inside the root
-  float x[8];
-  unpack_bf16x8(raw, x);
-  float sum = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) sum = __fadd_rn(sum, x[j]);
-  const float mean = __fmul_rn(halfwarp_sum(sum), 1.0f / kD);
-  float sq = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    x[j] = __fsub_rn(x[j], mean);
-    sq = __fmaf_rn(x[j], x[j], sq);
-  }
-  const float var = __fmul_rn(halfwarp_sum(sq), 1.0f / kD);
-  const float rstd = __frsqrt_rn(__fadd_rn(var, p.eps));
-#pragma unroll
-  for (int j = 0; j < 8; ++j) x[j] = __fmaf_rn(__fmul_rn(x[j], rstd), g[j], bt[j]);
-
-  rope_apply<STYLE>(x, R);
-  const int e = ue8m0_exponent(x);
-  const uint2 codes = quantize8(x, e);
-
-  if (!real) return;
-  if (!hd.pos_ok) {
-    if (l16 == 0) raise_error(p, DSA_DEVERR_POSITION);
-    return;
-  }
-  const long long slot = hd.slot;
-  if (slot < 0 || slot >= p.num_slots) {
-    if (l16 == 0) raise_error(p, DSA_DEVERR_SLOT);
-    return;
-  }
-  const long long page = slot / p.page_size;
-  const long long off = slot - page * p.page_size;
-  uint8_t* base = p.cache + page * p.page_bytes;
-  *reinterpret_cast<uint2*>(base + off * kD + 8 * l16) = codes;
-  if (l16 == 0)
-    *reinterpret_cast<float*>(base + static_cast<long long>(p.page_size) * kD + 4 * off) = pow2f(e);
-}
-
-template <int STYLE>
+template <int STYLE, int RP>
 __device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t full0,
                          uint32_t empty0, volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
-  const int hw = lane >> 4;
-  const int l16 = lane & 15;
+  const int qtr = lane >> 3;
+  const int l = lane & 7;
   int i = 0;
   for (long long u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
     const int s = i % kStages;
@@ -495,42 +761,48 @@ __device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t 
       }
       return;
     }
-    const StageHeader hd = *reinterpret_cast<const StageHeader*>(st + kOffHdr);
+    const StageHeader* hd = reinterpret_cast<const StageHeader*>(st + kOffHdr);
+    const bool pos_ok = hd->pos_ok != 0;
     const long long t = u / p.NC;
     const int c = static_cast<int>(u - t * p.NC);
     const int h0 = c * p.HC;
     const int n = min(p.HC, p.H - h0);
 
-    Rot R;
-    load_rot<STYLE>(R, sts, l16, p.rope_dim);
-
-    // query heads: warp cw takes head pairs cw, cw + kConsumers, ...
-    for (int pr = cw; 2 * pr < n; pr += kConsumers) {
-      const int v = 2 * pr + hw;
+    Rot<RP> r;
+    if constexpr (RP > 0) {
+      load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(sts + kOffCos + 4 * RP * l, r.c);
+      load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(sts + kOffSin + 4 * RP * l, r.s);
+      finish_rot<RP>(r);
+    }
+    const long long orow0 = t * p.H + h0;
+    // query heads: warp cw takes head quads cw, cw + kConsumers, ...
+    for (int qd = cw; 4 * qd < n; qd += kConsumers) {
+      const int v = 4 * qd + qtr;
       const bool valid = v < n;
+      float x[16] = {};
+      if (valid) load_slice<STYLE, RP, SharedMem>(sts + kOffQ + 256 * v, l, x);
       float wv = 0.0f;
-      if (valid && l16 == 0)
-        wv = p.w_bulk ? bf16_to_f32(*reinterpret_cast<const uint16_t*>(st + kOffW + 2 * v))
-                      : bf16_to_f32(__ldg(p.w + t * p.sw_t + h0 + v));
-      const uint4 raw = valid ? ld_shared16(sts + kOffQ + 256 * v + 16 * l16) : make_uint4(0, 0, 0, 0);
-      uint2 codes;
-      const int e = q_vector<STYLE>(raw, R, codes);
-      if (valid && hd.pos_ok) {
-        const long long row = t * p.H + h0 + v;
-        st_stream8(p.q_out + row * kD + 8 * l16, codes);
-        if (l16 == 0) __stcs(p.w_out + row, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold));
-      }
+      if (valid && l == 0)
+        wv = p.w_bulk ? __uint_as_float(static_cast<uint32_t>(
+                            *reinterpret_cast<const uint16_t*>(st + kOffW + 2 * v)) << 16)
+                      : __uint_as_float(static_cast<uint32_t>(__ldg(p.w + t * p.sw_t + h0 + v)) << 16);
+      const int e = q_slice<STYLE, RP>(x, r, p.q_out + (orow0 + v) * kD, l, valid && pos_ok);
+      if (valid && pos_ok && l == 0)
+        __stcs(p.w_out + orow0 + v, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold));
     }
     // the key rides with chunk 0; the warp that takes it rotates per unit
-    if (c == 0 && cw == i % kConsumers) k_vector<STYLE>(p, sts, hd, R, hw == 0, l16);
-
+    if (c == 0 && cw == i % kConsumers) {
+      float x[16];
+      load_slice<STYLE, RP, SharedMem>(sts + kOffK, l, x);
+      k_slice<STYLE, RP>(p, x, r, l, qtr == 0, pos_ok, hd->slot);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
   }
 }
 
-template <int STYLE>
-__global__ void __launch_bounds__(kThreads) dsa_prepare_store_kernel(const Params p) {
+template <int STYLE, int RP>
+__global__ void __launch_bounds__(kPipeThreads) dsa_pipeline_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
@@ -554,7 +826,7 @@ __global__ void __launch_bounds__(kThreads) dsa_prepare_store_kernel(const Param
   if (warp == 0)
     producer(p, ring, full0, empty0, abort_flag);
   else
-    consumer<STYLE>(p, warp - 1, ring, full0, empty0, abort_flag);
+    consumer<STYLE, RP>(p, warp - 1, ring, full0, empty0, abort_flag);
 }
 
 // ---------------------------------------------------------------- host side
@@ -563,17 +835,45 @@ bool misaligned(const void* ptr, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
 }
 
-// Per-device facts looked up once: SM count, and whether the kernels' dynamic
-// shared-memory limit has been raised on that device.
+using KernelFn = void (*)(Params);
+
+template <int STYLE, int RP>
+constexpr KernelFn pipeline_fn() { return dsa_pipeline_kernel<STYLE, RP>; }
+template <int STYLE, int RP>
+constexpr KernelFn direct_fn() { return dsa_direct_kernel<STYLE, RP>; }
+
+// rope_dim / 16 in {0, 1, 2, 4, 8} -> table index
+int rp_index(int rope_dim) {
+  switch (rope_dim) {
+    case 0: return 0;
+    case 16: return 1;
+    case 32: return 2;
+    case 64: return 3;
+    case 128: return 4;
+  }
+  return -1;
+}
+
+const KernelFn kPipeline[2][5] = {
+    {pipeline_fn<0, 0>(), pipeline_fn<0, 1>(), pipeline_fn<0, 2>(), pipeline_fn<0, 4>(),
+     pipeline_fn<0, 8>()},
+    {pipeline_fn<1, 0>(), pipeline_fn<1, 1>(), pipeline_fn<1, 2>(), pipeline_fn<1, 4>(),
+     pipeline_fn<1, 8>()}};
+const KernelFn kDirect[2][5] = {
+    {direct_fn<0, 0>(), direct_fn<0, 1>(), direct_fn<0, 2>(), direct_fn<0, 4>(), direct_fn<0, 8>()},
+    {direct_fn<1, 0>(), direct_fn<1, 1>(), direct_fn<1, 2>(), direct_fn<1, 4>(), direct_fn<1, 8>()}};
+
+int max_pipeline_smem() { return kBarrierBytes + kStages * (kOffQ + kHCMax * 256); }
+
+// Per-device facts looked up once: the SM count, and whether the pipeline
+// kernels' dynamic shared-memory limit has been raised on that device.
 struct DeviceInfo {
   int sms = 0;
-  bool smem_set = false;
+  bool ready = false;
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
-
-int max_smem_bytes() { return kBarrierBytes + kStages * (kOffQ + kHCMax * 256); }
 
 cudaError_t device_info(int* sms) {
   int dev = 0;
@@ -582,26 +882,28 @@ cudaError_t device_info(int* sms) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_dev_mu);
   DeviceInfo& d = g_dev[dev];
-  if (!d.smem_set) {
+  if (!d.ready) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(dsa_prepare_store_kernel<DSA_ROPE_NEOX>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_bytes());
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(dsa_prepare_store_kernel<DSA_ROPE_GPTJ>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_bytes());
-    if (e != cudaSuccess) return e;
-    d.smem_set = true;
+    for (int s = 0; s < 2; ++s)
+      for (int r = 0; r < 5; ++r) {
+        e = cudaFuncSetAttribute(kPipeline[s][r], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 max_pipeline_smem());
+        if (e != cudaSuccess) return e;
+      }
+    d.ready = true;
   }
   *sms = d.sms;
   return cudaSuccess;
 }
 
-// Heads per unit: whole tokens (HC = H, up to 64) when there are enough tokens
-// to fill the machine; for small T the heads are split (down to 8 per unit)
-// until the units cover the SMs.
-// Chunks hold a multiple of 8 heads when H >= 8, so every chunk's weights start
-// on a 16-byte boundary and can ride the bulk copies (when w itself allows).
+// Calls up to this many query vectors (T * H) take the direct kernel.
+constexpr long long kDirectMaxVectors = 16384;
+
+// Pipeline units: whole tokens (HC = H, up to 64) when there are enough tokens
+// to fill the machine; otherwise heads are split (chunks of >= 8) until the
+// units cover the SMs.  Chunks hold a multiple of 8 heads when H >= 8, so each
+// chunk's weights start on a 16-byte boundary and can ride the bulk copies.
 void choose_units(Params& p, int sms, bool w_rows_aligned) {
   if (p.H == 0) {
     p.HC = 0;
@@ -626,27 +928,38 @@ cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligne
   int sms = 0;
   cudaError_t e = device_info(&sms);
   if (e != cudaSuccess) return e;
-  choose_units(p, sms, w_rows_aligned);
-  const int smem = kBarrierBytes + kStages * p.stage_bytes;
-  const int per_sm = p.HC >= 32 ? 3 : 6;
-  long long blocks = static_cast<long long>(sms) * per_sm;
-  if (blocks > p.units) blocks = p.units;
+  const int ri = rp_index(p.rope_dim);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  cfg.numAttrs = 0;
   if (flags & DSA_FLAG_PDL) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return rope_style == DSA_ROPE_NEOX
-             ? cudaLaunchKernelEx(&cfg, dsa_prepare_store_kernel<DSA_ROPE_NEOX>, p)
-             : cudaLaunchKernelEx(&cfg, dsa_prepare_store_kernel<DSA_ROPE_GPTJ>, p);
+  const long long vecs = static_cast<long long>(p.T) * (p.H > 0 ? p.H : 1);
+  bool direct = vecs <= kDirectMaxVectors;
+  if (flags & DSA_FLAG_PIPELINE) direct = false;
+  if (flags & DSA_FLAG_DIRECT) direct = true;
+  if (direct) {
+    p.NQ = (p.H + 3) / 4;
+    p.q_warps = static_cast<long long>(p.T) * p.NQ;
+    p.k_warps = (static_cast<long long>(p.T) + 3) / 4;
+    const long long warps = p.q_warps + p.k_warps;
+    cfg.gridDim = dim3(static_cast<unsigned>((warps + kDirectThreads / 32 - 1) / (kDirectThreads / 32)));
+    cfg.blockDim = dim3(kDirectThreads);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, kDirect[rope_style][ri], p);
+  }
+  choose_units(p, sms, w_rows_aligned);
+  const int per_sm = p.HC >= 32 ? 3 : 6;
+  long long blocks = static_cast<long long>(sms) * per_sm;
+  if (blocks > p.units) blocks = p.units;
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kPipeThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(kBarrierBytes + kStages * p.stage_bytes);
+  return cudaLaunchKernelEx(&cfg, kPipeline[rope_style][ri], p);
 }
 
 dsa_status check_k_side(const void* k, int64_t k_stride_t, const int64_t* positions,
@@ -658,9 +971,11 @@ dsa_status check_k_side(const void* k, int64_t k_stride_t, const int64_t* positi
                         uint32_t flags) {
   if (T < 0) return DSA_ERR_SHAPE;
   if (head_dim != kD) return DSA_ERR_UNSUPPORTED;
-  if (rope_dim < 0 || rope_dim > kD || rope_dim % 16 != 0) return DSA_ERR_UNSUPPORTED;
+  if (rp_index(rope_dim) < 0) return DSA_ERR_UNSUPPORTED;
   if (rope_style != DSA_ROPE_NEOX && rope_style != DSA_ROPE_GPTJ) return DSA_ERR_UNSUPPORTED;
-  if (flags & ~static_cast<uint32_t>(DSA_FLAG_PDL)) return DSA_ERR_UNSUPPORTED;
+  if (flags & ~static_cast<uint32_t>(DSA_FLAG_PDL | DSA_FLAG_PIPELINE | DSA_FLAG_DIRECT))
+    return DSA_ERR_UNSUPPORTED;
+  if ((flags & DSA_FLAG_PIPELINE) && (flags & DSA_FLAG_DIRECT)) return DSA_ERR_UNSUPPORTED;
   if (!(ln_eps >= 0.0f) || !std::isfinite(ln_eps)) return DSA_ERR_UNSUPPORTED;
   if (page_size < 1 || num_pages < 1 || max_position < 1) return DSA_ERR_SHAPE;
   if (num_pages > INT64_MAX / (static_cast<int64_t>(page_size) * (kD + 4)))
@@ -784,6 +1099,6 @@ const char* dsa_status_string(dsa_status status) {
   return "unknown status";
 }
 
-int32_t dsa_prep_version(void) { return (2 << 16) | 0; }
+int32_t dsa_prep_version(void) { return (3 << 16) | 0; }
 
 }  // extern "C"
