@@ -16,9 +16,11 @@ kernel launch.  Prints ONE JSON line (rank 0):
              copy bandwidth; traffic = DRAM bytes per launch from the committed
              ncu summary when it was taken on the current kernel source
   decode     us per call at the decode shapes (T = 64, H = 64, GPT-J; and
-             T in {1, 8, 32, 64, 256}, H = 32, NeoX), graph-replayed (21 calls on
-             21 distinct input sets per graph, L2 flushed before each replay)
-             and eager
+             T in {1, 8, 32, 64, 256}, H = 32, NeoX): one decode step of 21
+             indexer layers (shared positions / slots / rope cache, per-layer
+             q, k|w, outputs and index-K cache) captured as a CUDA graph and
+             replayed after an L2 flush -- plain, with PDL, and with PDL plus
+             early rope reads -- plus a single-call graph and eager calls
   cpu_baseline  the oracle (plain C, one core) on a bounded sample
 
 ``--impl reference`` times the oracle instead (the CPU statement of the path),
@@ -174,17 +176,29 @@ def _call(dp, inp, d, stream, T=None, k_only=False, pdl=False):
         max_position=inp.max_position, stream=stream, num_tokens=T, pdl=pdl)
 
 
-def _decode_timings(dp, torch, dev, make, label, reps=30, layers=21, k_only_too=False):
-    """us/call: a graph of `layers` sequential calls on distinct input sets,
-    replayed `reps` times with an L2 flush before each replay (only the replay
-    is timed); a single-call graph; eager back-to-back calls."""
+def _decode_timings(dp, torch, dev, make, reps=30, layers=21, k_only_too=False):
+    """us per call for one decode step of `layers` indexer layers: the layers
+    share the step's positions, slots and rope cache (as in a model) and each
+    has its own q, k|w, outputs and index-K cache.  Timed as a graph of the
+    `layers` sequential calls replayed `reps` times with an L2 flush before
+    each replay (only the replay is timed) -- plain, with programmatic
+    dependent launch, and with PDL plus early reads of positions / cos / sin --
+    and as a single-call graph and back-to-back eager calls."""
+    base = make(0)
+    shared = None
     sets = []
     for i in range(layers):
-        inp = make(i)
-        sets.append((inp, _dev_inputs(inp, dev)))
+        inp = base if i == 0 else make(i)
+        d = _dev_inputs(inp, dev)
+        if shared is None:
+            shared = {k: d[k] for k in ("positions", "slots", "cos", "sin")}
+        d.update(shared)
+        inp.positions, inp.slots, inp.cos, inp.sin = base.positions, base.slots, base.cos, base.sin
+        inp.max_position = base.max_position
+        sets.append((inp, d))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    out = {"T": sets[0][0].T, "H": sets[0][0].H, "style": "gptj" if sets[0][0].style else "neox"}
+    out = {"T": base.T, "H": base.H, "style": "gptj" if base.style else "neox"}
     modes = [("qk", False)] + ([("k_only", True)] if k_only_too else [])
     for name, k_only in modes:
         with torch.cuda.stream(stream):
@@ -192,7 +206,10 @@ def _decode_timings(dp, torch, dev, make, label, reps=30, layers=21, k_only_too=
                 _call(dp, inp, d, stream, k_only=k_only)
         stream.synchronize()
         res = {}
-        for n_layers, pdl in ((layers, False), (layers, True), (1, False)):
+        for n_layers, pdl, key in ((layers, False, f"graph{layers}_us"),
+                                   (layers, True, f"graph{layers}_pdl_us"),
+                                   (layers, "early", f"graph{layers}_pdl_early_us"),
+                                   (1, False, "graph1_us")):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for inp, d in sets[:n_layers]:
@@ -208,7 +225,6 @@ def _decode_timings(dp, torch, dev, make, label, reps=30, layers=21, k_only_too=
                     e1.record(stream)
                 stream.synchronize()
                 times.append(e0.elapsed_time(e1) * 1000.0 / n_layers)
-            key = f"graph{n_layers}{'_pdl' if pdl else ''}_us"
             res[key] = {"median": statistics.median(times), "best": min(times)}
             del g
         # eager: back-to-back calls through the Python binding
@@ -342,10 +358,10 @@ def run_ours(args, rank, world, local_rank):
     decode = None
     if rank == 0 and not args.no_decode:
         decode = {"c2_decode_T64_H64_gptj": _decode_timings(
-            dp, torch, dev, lambda i: synth.make_decode(seed=1 + 100 * i), "c2", k_only_too=True)}
+            dp, torch, dev, lambda i: synth.make_decode(seed=1 + 100 * i), k_only_too=True)}
         for Tn in (1, 8, 32, 64, 256):
             decode[f"sweep_T{Tn}_H32"] = _decode_timings(
-                dp, torch, dev, lambda i, Tn=Tn: synth.make_sweep(Tn, seed=2 + 100 * i), "c3")
+                dp, torch, dev, lambda i, Tn=Tn: synth.make_sweep(Tn, seed=2 + 100 * i))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -100,6 +100,14 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
  * bytes.  Setting both is an error. */
 #define DSA_FLAG_PIPELINE 2u
 #define DSA_FLAG_DIRECT 4u
+/* With DSA_FLAG_PDL only: the caller promises that positions, out_cache_loc
+ * and the cos/sin cache are NOT written by the kernel that precedes this call
+ * in the stream (true in a decode step, where they are set up before the
+ * layers run).  The kernel then reads them -- and fetches the cos/sin rows
+ * they select -- before it waits for that kernel, overlapping two dependent
+ * memory round trips with its tail.  q, k and w are still read only after the
+ * wait.  Without DSA_FLAG_PDL this flag is an error. */
+#define DSA_FLAG_PDL_EARLY_ROPE 8u
 
 /*
  * Fused Q/K prepare-and-store: returns the (q_fp8, weights) contract and

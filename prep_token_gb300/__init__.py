@@ -24,7 +24,7 @@ from ._build import LIB_PATH
 
 __all__ = [
     "DsaError", "NEOX", "GPTJ", "HEAD_DIM", "DEVERR_POSITION", "DEVERR_SLOT", "DEVERR_TIMEOUT",
-    "FLAG_PDL", "FLAG_PIPELINE", "FLAG_DIRECT",
+    "FLAG_PDL", "FLAG_PIPELINE", "FLAG_DIRECT", "FLAG_PDL_EARLY_ROPE",
     "dsa_indexer_qk_prepare_store", "dsa_indexer_k_prepare_store", "dsa_status_string",
     "library", "cache_bytes", "cache_views",
 ]
@@ -32,7 +32,7 @@ __all__ = [
 NEOX, GPTJ = 0, 1
 HEAD_DIM = 128
 DEVERR_POSITION, DEVERR_SLOT, DEVERR_TIMEOUT = 1, 2, 4
-FLAG_PDL, FLAG_PIPELINE, FLAG_DIRECT = 1, 2, 4
+FLAG_PDL, FLAG_PIPELINE, FLAG_DIRECT, FLAG_PDL_EARLY_ROPE = 1, 2, 4, 8
 _KERNEL_FLAGS = {"auto": 0, "pipeline": FLAG_PIPELINE, "direct": FLAG_DIRECT}
 ROW_BYTES = HEAD_DIM + 4  # 128 codes + one fp32 scale per slot
 
@@ -120,10 +120,17 @@ def _num_pages(index_k_cache: torch.Tensor, page_size: int) -> int:
     return nbytes // (page_size * ROW_BYTES)
 
 
-def _flags(pdl: bool, kernel: str) -> int:
+def _flags(pdl, kernel: str) -> int:
+    """pdl: False, True, or "early" (PDL plus FLAG_PDL_EARLY_ROPE: positions,
+    slots and the cos/sin cache are not written by the previous kernel)."""
     if kernel not in _KERNEL_FLAGS:
         raise ValueError(f"kernel must be one of {sorted(_KERNEL_FLAGS)}")
-    return (FLAG_PDL if pdl else 0) | _KERNEL_FLAGS[kernel]
+    if pdl not in (False, True, "early"):
+        raise ValueError('pdl must be False, True or "early"')
+    f = FLAG_PDL if pdl else 0
+    if pdl == "early":
+        f |= FLAG_PDL_EARLY_ROPE
+    return f | _KERNEL_FLAGS[kernel]
 
 
 def _stream(stream) -> int:
@@ -166,7 +173,9 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
     ``num_tokens`` limits the call to the first T live tokens (the graph
     split-op contract); outputs are sized to it.  ``pdl`` launches with
     programmatic dependent launch (the kernel may start while the previous
-    kernel of the stream drains; it still waits for that kernel's memory).
+    kernel of the stream drains; it still waits for that kernel's memory);
+    ``pdl="early"`` also reads positions, slots and cos/sin before that wait
+    (only when the previous kernel does not write them).
     ``kernel`` = "auto" | "direct" | "pipeline" overrides the size-based
     choice between the two kernels (same bytes either way).
     Returns (q_fp8 [T, H, 128] float8_e4m3fn, weights [T, H] fp32)."""

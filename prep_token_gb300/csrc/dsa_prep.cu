@@ -84,6 +84,7 @@ struct Params {
   int NQ;            // quads of heads per token
   long long q_warps;  // warps doing q quads
   long long k_warps;  // warps doing keys (four per warp)
+  int early_rope;     // read positions and cos/sin before the PDL wait
   int* err;
 };
 
@@ -589,22 +590,42 @@ __device__ __forceinline__ void load_rot_global(const Params& p, long long row, 
   }
 }
 
+// Position-dependent prologue of a token: its position, whether it is in
+// range, and the lane's cos/sin values.
+template <int RP>
+__device__ __forceinline__ bool token_rot(const Params& p, long long t, int l, long long& pos,
+                                          Rot<RP>& r) {
+  pos = __ldg(p.pos + t);
+  const bool pos_ok = pos >= 0 && pos < p.max_pos;
+  load_rot_global<RP>(p, pos_ok ? pos : 0, l, r);
+  return pos_ok;
+}
+
 template <int STYLE, int RP>
 __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params p) {
-  grid_dependency_wait();
-  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int qtr = lane >> 3;
   const int l = lane & 7;
   const long long u = static_cast<long long>(blockIdx.x) * (kDirectThreads / 32) + (threadIdx.x >> 5);
+  const bool is_q = u < p.q_warps;
+  // q warp: four heads of one token; k warp: four keys, one per quarter-warp
+  const long long t = is_q ? u / p.NQ : 4 * (u - p.q_warps) + qtr;
+  const bool real = is_q || t < p.T;
+  const long long tt = real ? t : 0;
+  long long pos = 0;
+  bool pos_ok = false;
+  Rot<RP> r;
+  // With DSA_FLAG_PDL_EARLY_ROPE the caller guarantees that positions, slots
+  // and the cos/sin cache are not written by the previous kernel in the
+  // stream, so their two dependent round trips overlap its tail.
+  if (p.early_rope && u < p.q_warps + p.k_warps) pos_ok = token_rot<RP>(p, tt, l, pos, r);
+  grid_dependency_wait();
+  grid_launch_dependents();
   if (u >= p.q_warps + p.k_warps) return;  // warp-uniform
 
-  if (u < p.q_warps) {
-    // four heads of one token
-    const long long t = u / p.NQ;
+  if (is_q) {
     const int v = static_cast<int>(u - t * p.NQ) * 4 + qtr;
     const bool valid = v < p.H;
-    const long long pos = __ldg(p.pos + t);
     float x[16] = {};
     if (valid) {
       const unsigned char* row = reinterpret_cast<const unsigned char*>(p.q + t * p.sq_t + v * p.sq_h);
@@ -612,24 +633,15 @@ __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params
     }
     float wv = 0.0f;
     if (valid && l == 0) wv = __uint_as_float(static_cast<uint32_t>(__ldg(p.w + t * p.sw_t + v)) << 16);
-    const bool pos_ok = pos >= 0 && pos < p.max_pos;
-    Rot<RP> r;
-    load_rot_global<RP>(p, pos_ok ? pos : 0, l, r);
+    if (!p.early_rope) pos_ok = token_rot<RP>(p, t, l, pos, r);
     const long long orow = t * p.H + v;
     const int e = q_slice<STYLE, RP>(x, r, p.q_out + orow * kD, l, valid && pos_ok);
     if (valid && pos_ok && l == 0) __stcs(p.w_out + orow, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold));
   } else {
-    // four keys, one per quarter-warp
-    const long long t = 4 * (u - p.q_warps) + qtr;
-    const bool real = t < p.T;
-    const long long tt = real ? t : 0;
-    const long long pos = __ldg(p.pos + tt);
-    const long long slot = __ldg(p.loc + tt);
     float x[16];
     load_slice<STYLE, RP, GlobalMem>(reinterpret_cast<const unsigned char*>(p.k + tt * p.sk_t), l, x);
-    const bool pos_ok = pos >= 0 && pos < p.max_pos;
-    Rot<RP> r;
-    load_rot_global<RP>(p, pos_ok ? pos : 0, l, r);
+    const long long slot = __ldg(p.loc + tt);
+    if (!p.early_rope) pos_ok = token_rot<RP>(p, tt, l, pos, r);
     k_slice<STYLE, RP>(p, x, r, l, real, pos_ok, slot);
   }
 }
@@ -663,8 +675,18 @@ __device__ void producer(const Params& p, unsigned char* ring, uint32_t full0, u
                          volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
   long long my_pos = 0, my_slot = 0;
+  // (token, chunk) of unit u, advanced incrementally as u steps by gridDim.x
+  const long long dt = gridDim.x / p.NC;
+  const int dc = static_cast<int>(gridDim.x - dt * p.NC);
+  long long t = blockIdx.x / p.NC;
+  int c = static_cast<int>(blockIdx.x - t * p.NC);
   int i = 0;
   for (long long u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+    if (i > 0) {
+      t += dt;
+      c += dc;
+      if (c >= p.NC) c -= p.NC, ++t;
+    }
     const int j = i & 31;
     if (j == 0) {
       const long long uu = u + static_cast<long long>(lane) * gridDim.x;
@@ -681,8 +703,6 @@ __device__ void producer(const Params& p, unsigned char* ring, uint32_t full0, u
     const uint32_t full = full0 + 8 * s;
     unsigned char* st = ring + static_cast<size_t>(s) * p.stage_bytes;
     const uint32_t sts = smem_u32(st);
-    const long long t = u / p.NC;
-    const int c = static_cast<int>(u - t * p.NC);
     if (lane == 0) {
       const uint32_t ph = (i / kStages) & 1;
       if (i >= kStages && !mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag)) {
@@ -747,8 +767,17 @@ __device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t 
   const int lane = threadIdx.x & 31;
   const int qtr = lane >> 3;
   const int l = lane & 7;
+  const long long dt = gridDim.x / p.NC;
+  const int dc = static_cast<int>(gridDim.x - dt * p.NC);
+  long long t = blockIdx.x / p.NC;
+  int c = static_cast<int>(blockIdx.x - t * p.NC);
   int i = 0;
   for (long long u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+    if (i > 0) {
+      t += dt;
+      c += dc;
+      if (c >= p.NC) c -= p.NC, ++t;
+    }
     const int s = i % kStages;
     const uint32_t ph = (i / kStages) & 1;
     unsigned char* st = ring + static_cast<size_t>(s) * p.stage_bytes;
@@ -763,8 +792,6 @@ __device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t 
     }
     const StageHeader* hd = reinterpret_cast<const StageHeader*>(st + kOffHdr);
     const bool pos_ok = hd->pos_ok != 0;
-    const long long t = u / p.NC;
-    const int c = static_cast<int>(u - t * p.NC);
     const int h0 = c * p.HC;
     const int n = min(p.HC, p.H - h0);
 
@@ -938,6 +965,7 @@ cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligne
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
+  p.early_rope = (flags & DSA_FLAG_PDL_EARLY_ROPE) ? 1 : 0;
   const long long vecs = static_cast<long long>(p.T) * (p.H > 0 ? p.H : 1);
   bool direct = vecs <= kDirectMaxVectors;
   if (flags & DSA_FLAG_PIPELINE) direct = false;
@@ -973,8 +1001,10 @@ dsa_status check_k_side(const void* k, int64_t k_stride_t, const int64_t* positi
   if (head_dim != kD) return DSA_ERR_UNSUPPORTED;
   if (rp_index(rope_dim) < 0) return DSA_ERR_UNSUPPORTED;
   if (rope_style != DSA_ROPE_NEOX && rope_style != DSA_ROPE_GPTJ) return DSA_ERR_UNSUPPORTED;
-  if (flags & ~static_cast<uint32_t>(DSA_FLAG_PDL | DSA_FLAG_PIPELINE | DSA_FLAG_DIRECT))
+  if (flags & ~static_cast<uint32_t>(DSA_FLAG_PDL | DSA_FLAG_PIPELINE | DSA_FLAG_DIRECT |
+                                     DSA_FLAG_PDL_EARLY_ROPE))
     return DSA_ERR_UNSUPPORTED;
+  if ((flags & DSA_FLAG_PDL_EARLY_ROPE) && !(flags & DSA_FLAG_PDL)) return DSA_ERR_UNSUPPORTED;
   if ((flags & DSA_FLAG_PIPELINE) && (flags & DSA_FLAG_DIRECT)) return DSA_ERR_UNSUPPORTED;
   if (!(ln_eps >= 0.0f) || !std::isfinite(ln_eps)) return DSA_ERR_UNSUPPORTED;
   if (page_size < 1 || num_pages < 1 || max_position < 1) return DSA_ERR_SHAPE;

@@ -249,9 +249,11 @@ def test_pdl_launch_matches():
     inp = synth.make_decode(seed=16, T=64, H=64)
     d = to_device(inp)
     plain = run_qk(inp, d)
-    pdl = run_qk(inp, d, pdl=True)
-    for key in ("q_fp8", "weights", "cache"):
-        assert np.array_equal(plain[key], pdl[key]), key
+    for mode in (True, "early"):
+        for kern in ("direct", "pipeline"):
+            pdl = run_qk(inp, d, pdl=mode, kernel=kern)
+            for key in ("q_fp8", "weights", "cache"):
+                assert np.array_equal(plain[key], pdl[key]), (key, mode, kern)
     import prep_token_gb300 as dp
     cache = new_cache(inp)
     q_out = torch.empty((64, 64, 128), dtype=torch.float8_e4m3fn, device="cuda")
@@ -265,7 +267,7 @@ def test_pdl_launch_matches():
                 d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"],
                 d["gamma"], d["beta"], inp.eps, inp.softmax_scale, cache, inp.page_size,
                 inp.rope_dim, inp.style, q_fp8_out=q_out, weights_out=w_out,
-                max_position=inp.max_position, pdl=True, stream=s)
+                max_position=inp.max_position, pdl="early", stream=s)
             dp.dsa_indexer_k_prepare_store(
                 d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
                 inp.eps, k_cache, inp.page_size, inp.rope_dim, inp.style,
