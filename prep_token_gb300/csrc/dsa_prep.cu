@@ -371,24 +371,6 @@ __device__ __forceinline__ void load_slice(typename M::Addr row, int l, float (&
   if constexpr (S::NP > 0) load_bf16<M, S::NP, S::ALIGN_P_BF16>(row + 2 * (S::P_BASE + S::NP * l), x + 2 * RP);
 }
 
-// The same slice of an fp32 row (LayerNorm gamma / beta).
-template <int STYLE, int RP>
-__device__ __forceinline__ void load_slice_f32(const float* row, int l, float (&x)[16]) {
-  using S = Slice<STYLE, RP>;
-  if constexpr (RP > 0) {
-    if constexpr (S::NEOX) {
-      load_f32_global<RP, S::ALIGN_A_F32>(row + RP * l, x);
-      load_f32_global<RP, S::ALIGN_B_F32>(row + S::B_BASE + RP * l, x + RP);
-    } else {
-      float t[2 * RP];
-      load_f32_global<2 * RP, S::ALIGN_A_F32>(row + 2 * RP * l, t);
-#pragma unroll
-      for (int j = 0; j < RP; ++j) x[j] = t[2 * j], x[RP + j] = t[2 * j + 1];
-    }
-  }
-  if constexpr (S::NP > 0) load_f32_global<S::NP, S::ALIGN_P_F32>(row + S::P_BASE + S::NP * l, x + 2 * RP);
-}
-
 // Rotation operands of the lane: frequencies RP*l .. RP*l + RP - 1.
 template <int RP>
 struct Rot {
@@ -534,12 +516,53 @@ __device__ __forceinline__ void raise_error(const Params& p, int bit) {
 
 // Key vector: LayerNorm (mean, biased variance, eps inside the root), RoPE,
 // quantise, and store the codes and the scale into slot `slot` of the cache.
+// y = x * rstd * gamma + beta on n values whose gamma/beta start at `row`
+// (fp32 [128] rows), one aligned piece at a time to keep few registers live.
+template <int N, int ALIGN>
+__device__ __forceinline__ void affine_piece(const float* g_row, const float* b_row, float* x,
+                                             float rstd) {
+  float g[N], b[N];
+  load_f32_global<N, ALIGN>(g_row, g);
+  load_f32_global<N, ALIGN>(b_row, b);
+#pragma unroll
+  for (int j = 0; j < N; ++j) x[j] = __fmaf_rn(__fmul_rn(x[j], rstd), g[j], b[j]);
+}
+
+template <int STYLE, int RP>
+__device__ __forceinline__ void affine_slice(const Params& p, int l, float (&x)[16], float rstd) {
+  using S = Slice<STYLE, RP>;
+  if constexpr (RP > 0) {
+    if constexpr (S::NEOX) {
+      affine_piece<RP, S::ALIGN_A_F32>(p.gamma + RP * l, p.beta + RP * l, x, rstd);
+      affine_piece<RP, S::ALIGN_B_F32>(p.gamma + S::B_BASE + RP * l, p.beta + S::B_BASE + RP * l,
+                                       x + RP, rstd);
+    } else {
+      float g[2 * RP], b[2 * RP];
+      load_f32_global<2 * RP, S::ALIGN_A_F32>(p.gamma + 2 * RP * l, g);
+      load_f32_global<2 * RP, S::ALIGN_A_F32>(p.beta + 2 * RP * l, b);
+#pragma unroll
+      for (int j = 0; j < RP; ++j) {
+        x[j] = __fmaf_rn(__fmul_rn(x[j], rstd), g[2 * j], b[2 * j]);
+        x[RP + j] = __fmaf_rn(__fmul_rn(x[RP + j], rstd), g[2 * j + 1], b[2 * j + 1]);
+      }
+    }
+  }
+  constexpr int NP = S::NP;
+  if constexpr (NP > 0) {
+    // pieces of at most 4 values
+    constexpr int PIECE = NP >= 4 ? 4 : NP;
+#pragma unroll
+    for (int j = 0; j < NP; j += PIECE) {
+      constexpr int A = S::ALIGN_P_F32 < 4 * PIECE ? S::ALIGN_P_F32 : 4 * PIECE;
+      affine_piece<PIECE, A>(p.gamma + S::P_BASE + NP * l + j, p.beta + S::P_BASE + NP * l + j,
+                             x + 2 * RP + j, rstd);
+    }
+  }
+}
+
 template <int STYLE, int RP>
 __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const Rot<RP>& r,
                                         int l, bool real, bool pos_ok, long long slot) {
-  float g[16], bt[16];
-  load_slice_f32<STYLE, RP>(p.gamma, l, g);
-  load_slice_f32<STYLE, RP>(p.beta, l, bt);
   float sum = 0.0f;
 #pragma unroll
   for (int j = 0; j < 16; ++j) sum = __fadd_rn(sum, x[j]);
@@ -552,8 +575,7 @@ __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const R
   }
   const float var = __fmul_rn(quad_sum(sq), 1.0f / kD);
   const float rstd = __frsqrt_rn(__fadd_rn(var, p.eps));
-#pragma unroll
-  for (int j = 0; j < 16; ++j) x[j] = __fmaf_rn(__fmul_rn(x[j], rstd), g[j], bt[j]);
+  affine_slice<STYLE, RP>(p, l, x, rstd);
   if constexpr (RP > 0) rope_slice<RP>(x, r);
   const int e = ue8m0_exponent(x);
   uint32_t wa[4], wb[4], wp[4];
@@ -676,10 +698,10 @@ __device__ void producer(const Params& p, unsigned char* ring, uint32_t full0, u
   const int lane = threadIdx.x & 31;
   long long my_pos = 0, my_slot = 0;
   // (token, chunk) of unit u, advanced incrementally as u steps by gridDim.x
-  const long long dt = gridDim.x / p.NC;
-  const int dc = static_cast<int>(gridDim.x - dt * p.NC);
-  long long t = blockIdx.x / p.NC;
-  int c = static_cast<int>(blockIdx.x - t * p.NC);
+  const int dt = static_cast<int>(gridDim.x) / p.NC;
+  const int dc = static_cast<int>(gridDim.x) - dt * p.NC;
+  int t = static_cast<int>(blockIdx.x) / p.NC;
+  int c = static_cast<int>(blockIdx.x) - t * p.NC;
   int i = 0;
   for (long long u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
     if (i > 0) {
@@ -767,10 +789,10 @@ __device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t 
   const int lane = threadIdx.x & 31;
   const int qtr = lane >> 3;
   const int l = lane & 7;
-  const long long dt = gridDim.x / p.NC;
-  const int dc = static_cast<int>(gridDim.x - dt * p.NC);
-  long long t = blockIdx.x / p.NC;
-  int c = static_cast<int>(blockIdx.x - t * p.NC);
+  const int dt = static_cast<int>(gridDim.x) / p.NC;
+  const int dc = static_cast<int>(gridDim.x) - dt * p.NC;
+  int t = static_cast<int>(blockIdx.x) / p.NC;
+  int c = static_cast<int>(blockIdx.x) - t * p.NC;
   int i = 0;
   for (long long u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
     if (i > 0) {
@@ -829,7 +851,7 @@ __device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t 
 }
 
 template <int STYLE, int RP>
-__global__ void __launch_bounds__(kPipeThreads) dsa_pipeline_kernel(const Params p) {
+__global__ void __launch_bounds__(kPipeThreads, 3) dsa_pipeline_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
