@@ -640,9 +640,11 @@ __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params
   // With DSA_FLAG_PDL_EARLY_ROPE the caller guarantees that positions, slots
   // and the cos/sin cache are not written by the previous kernel in the
   // stream, so their two dependent round trips overlap its tail.
+  // Let the next kernel of the stream get its CTAs resident now: it waits for
+  // this grid's completion on its own griddepcontrol.wait.
+  grid_launch_dependents();
   if (p.early_rope && u < p.q_warps + p.k_warps) pos_ok = token_rot<RP>(p, tt, l, pos, r);
   grid_dependency_wait();
-  grid_launch_dependents();
   if (u >= p.q_warps + p.k_warps) return;  // warp-uniform
 
   if (is_q) {
