@@ -45,7 +45,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "tokens/s + achieved HBM GB/s (% of peak) prefill; µs/call at decode T=1..64"
 WORKLOAD = "prefill T=8192 H=64 D=128 rope_dim=64 NeoX, 128 pages x 64 (contiguous slots)"
-PROFILE = os.path.join(ROOT, "profiles", "dsa_prepare_store_prefill_T8192_H64.md")
+PROFILE = os.path.join(ROOT, "profiles", "dsa_pipeline_kernel_prefill_T8192_H64.md")
 KERNEL_SRC = os.path.join(ROOT, "prep_token_gb300", "csrc", "dsa_prep.cu")
 L2_FLUSH_BYTES = 256 << 20
 GRAPH_STEPS = 50
@@ -483,6 +483,22 @@ def run_reference(args, rank, world):
     }
 
 
+def run_probe(which, local_rank):
+    """A few eager calls on one workload, for ncu captures (no timing, no JSON)."""
+    import torch
+    import prep_token_gb300 as dp
+    import synth
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp = synth.make_decode(seed=1) if which == "decode" else synth.make_prefill(seed=3)
+    d = _dev_inputs(inp, dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(6):
+        _call(dp, inp, d, stream)
+    torch.cuda.synchronize(dev)
+    print(f"probe {which}: 6 calls (T={inp.T}, H={inp.H})")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -492,6 +508,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--probe", choices=("prefill", "decode"),
+                    help="make 6 eager calls on that workload and exit (for profilers)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -499,6 +517,9 @@ def main():
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)
     local_rank = _env_int("LOCAL_RANK", 0)
+    if args.probe:
+        run_probe(args.probe, local_rank)
+        return
     if args.impl == "reference":
         out = run_reference(args, rank, world)
     else:
