@@ -21,6 +21,9 @@ kernel launch.  Prints ONE JSON line (rank 0):
              q, k|w, outputs and index-K cache) captured as a CUDA graph and
              replayed after an L2 flush -- plain, with PDL, and with PDL plus
              early rope reads -- plus a single-call graph and eager calls
+  unfused    the same call as four launches with bf16 intermediates (the
+             pages' pre-fusion chain) on the prefill inputs and in the decode
+             step, for the 4 -> 1 launch comparison
   cpu_baseline  the oracle (plain C, one core) on a bounded sample
 
 ``--impl reference`` times the oracle instead (the CPU statement of the path),
@@ -162,7 +165,19 @@ def _dev_inputs(inp, dev):
     return d
 
 
-def _call(dp, inp, d, stream, T=None, k_only=False, pdl=False):
+def _add_workspace(dp, torch, inp, d, dev):
+    d["ws"] = torch.empty(dp.dsa_unfused_workspace_bytes(inp.T, inp.H), dtype=torch.uint8,
+                          device=dev)
+
+
+def _call(dp, inp, d, stream, T=None, k_only=False, pdl=False, unfused=False):
+    if unfused:
+        dp.dsa_indexer_qk_prepare_store_unfused(
+            d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
+            d["beta"], inp.eps, inp.softmax_scale, d["cache"], inp.page_size, inp.rope_dim,
+            inp.style, q_fp8_out=d["q_out"], weights_out=d["w_out"], workspace=d["ws"],
+            max_position=inp.max_position, stream=stream, num_tokens=T, pdl=bool(pdl))
+        return
     if k_only:
         dp.dsa_indexer_k_prepare_store(
             d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
@@ -176,7 +191,8 @@ def _call(dp, inp, d, stream, T=None, k_only=False, pdl=False):
         max_position=inp.max_position, stream=stream, num_tokens=T, pdl=pdl)
 
 
-def _decode_timings(dp, torch, dev, make, reps=30, layers=21, k_only_too=False):
+def _decode_timings(dp, torch, dev, make, reps=30, layers=21, k_only_too=False,
+                    unfused_too=False):
     """us per call for one decode step of `layers` indexer layers: the layers
     share the step's positions, slots and rope cache (as in a model) and each
     has its own q, k|w, outputs and index-K cache.  Timed as a graph of the
@@ -199,21 +215,25 @@ def _decode_timings(dp, torch, dev, make, reps=30, layers=21, k_only_too=False):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
     out = {"T": base.T, "H": base.H, "style": "gptj" if base.style else "neox"}
-    modes = [("qk", False)] + ([("k_only", True)] if k_only_too else [])
-    for name, k_only in modes:
+    modes = [("qk", False, False)] + ([("k_only", True, False)] if k_only_too else []) + \
+        ([("unfused_qk", False, True)] if unfused_too else [])
+    if unfused_too:
+        for inp, d in sets:
+            _add_workspace(dp, torch, inp, d, dev)
+    for name, k_only, unfused in modes:
         with torch.cuda.stream(stream):
             for inp, d in sets:          # warm-up outside capture
-                _call(dp, inp, d, stream, k_only=k_only)
+                _call(dp, inp, d, stream, k_only=k_only, unfused=unfused)
         stream.synchronize()
-        res = {}
-        for n_layers, pdl, key in ((layers, False, f"graph{layers}_us"),
-                                   (layers, True, f"graph{layers}_pdl_us"),
-                                   (layers, "early", f"graph{layers}_pdl_early_us"),
-                                   (1, False, "graph1_us")):
+        res = {"launches_per_call": 4 if unfused else 1}
+        variants = ((layers, False, f"graph{layers}_us"), (layers, True, f"graph{layers}_pdl_us"))
+        if not unfused:
+            variants += ((layers, "early", f"graph{layers}_pdl_early_us"), (1, False, "graph1_us"))
+        for n_layers, pdl, key in variants:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for inp, d in sets[:n_layers]:
-                    _call(dp, inp, d, stream, k_only=k_only, pdl=pdl)
+                    _call(dp, inp, d, stream, k_only=k_only, pdl=pdl, unfused=unfused)
             times = []
             for _ in range(reps):
                 with torch.cuda.stream(stream):
@@ -236,7 +256,7 @@ def _decode_timings(dp, torch, dev, make, reps=30, layers=21, k_only_too=False):
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 for inp, d in sets:
-                    _call(dp, inp, d, stream, k_only=k_only)
+                    _call(dp, inp, d, stream, k_only=k_only, unfused=unfused)
                 e1.record(stream)
                 stream.synchronize()
                 times.append(e0.elapsed_time(e1) * 1000.0 / len(sets))
@@ -355,10 +375,43 @@ def run_ours(args, rank, world, local_rank):
     h2d = h_q.numel() * 2 + h_kw.numel() * 2 + h_pos.numel() * 8 + h_slots.numel() * 8
     d2h = h_qo.numel() + h_wo.numel() * 4
 
+    # the unfused four-launch chain on the same prefill inputs (baseline)
+    unfused = None
+    if not args.no_unfused:
+        for inp, d in sets:
+            _add_workspace(dp, torch, inp, d, dev)
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                _call(dp, sets[i & 1][0], sets[i & 1][1], stream, unfused=True)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(10):
+                _call(dp, sets[i & 1][0], sets[i & 1][1], stream, unfused=True)
+        reps = max(1, min(100, args.steps // 10))
+        with torch.cuda.stream(stream):
+            g.replay()
+            u0 = torch.cuda.Event(enable_timing=True)
+            u1 = torch.cuda.Event(enable_timing=True)
+            u0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            u1.record(stream)
+        stream.synchronize()
+        del g
+        uus = u0.elapsed_time(u1) * 1000.0 / (10 * reps)
+        for _, d in sets:
+            del d["ws"]
+        unfused = {"prefill_us": uus, "launches_per_call": 4, "calls": 10 * reps,
+                   "fused_speedup": uus / launch_us,
+                   "hbm_bytes_per_call": synth.algorithmic_bytes(T, H)
+                   + T * (H + 1) * 128 * 2 * 2 + T * 128 * 2 * 2}
+
     decode = None
     if rank == 0 and not args.no_decode:
         decode = {"c2_decode_T64_H64_gptj": _decode_timings(
-            dp, torch, dev, lambda i: synth.make_decode(seed=1 + 100 * i), k_only_too=True)}
+            dp, torch, dev, lambda i: synth.make_decode(seed=1 + 100 * i), k_only_too=True,
+            unfused_too=True)}
         for Tn in (1, 8, 32, 64, 256):
             decode[f"sweep_T{Tn}_H32"] = _decode_timings(
                 dp, torch, dev, lambda i, Tn=Tn: synth.make_sweep(Tn, seed=2 + 100 * i))
@@ -402,6 +455,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
         "decode": decode,
+        "unfused": unfused,
         "cpu_baseline": cpu,
     }
 
@@ -507,6 +561,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--probe", choices=("prefill", "decode"),
                     help="make 6 eager calls on that workload and exit (for profilers)")

@@ -64,6 +64,7 @@
 #ifndef DSA_PREP_H
 #define DSA_PREP_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -165,6 +166,38 @@ dsa_status dsa_indexer_k_prepare_store(
     void* index_k_cache, int64_t num_pages, int32_t page_size,
     int32_t T, int32_t head_dim, int32_t rope_dim, int32_t rope_style,
     uint32_t flags, int32_t* err_flags, void* stream);
+
+/*
+ * The unfused chain: the same computation as dsa_indexer_qk_prepare_store,
+ * as the four launches per layer that the sglang PR "[AMD] [GLM5] Fuse the
+ * DSA indexer Q/K rope + quant + K-cache write" profiles before fusing
+ * (Profile section: rope q+k, LayerNorm, act_quant, k quant + cache; the gate
+ * fold rides with the q quant here).  Launch order: LayerNorm(k) -> RoPE(q, k)
+ * -> quant(q) + fold -> quant(k) + cache store.  The tensors between launches
+ * are bf16, kept in `workspace` (device memory owned by the caller, 256-byte
+ * aligned, at least dsa_unfused_workspace_bytes(T, H) bytes, contents
+ * scratch).  Because LayerNorm and RoPE outputs are rounded to bf16, its codes
+ * can differ from the fused call's by one step near rounding boundaries; its
+ * scales and slots follow the same rules.  Arguments and checks are those of
+ * dsa_indexer_qk_prepare_store; flags may hold DSA_FLAG_PDL only.  Kept as the
+ * baseline the fused call is measured against.
+ */
+size_t dsa_unfused_workspace_bytes(int32_t T, int32_t H);
+
+dsa_status dsa_indexer_qk_prepare_store_unfused(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    const void* k, int64_t k_stride_t,
+    const void* w, int64_t w_stride_t,
+    const int64_t* positions, const int64_t* out_cache_loc,
+    const float* cos_cache, const float* sin_cache, int64_t cs_stride,
+    int64_t max_position,
+    const float* ln_gamma, const float* ln_beta, float ln_eps,
+    float softmax_scale,
+    void* q_fp8_out, float* weights_out,
+    void* index_k_cache, int64_t num_pages, int32_t page_size,
+    int32_t T, int32_t H, int32_t head_dim, int32_t rope_dim,
+    int32_t rope_style, uint32_t flags, void* workspace, size_t workspace_bytes,
+    int32_t* err_flags, void* stream);
 
 /* A static, NUL-terminated description of a status code. */
 const char* dsa_status_string(dsa_status status);

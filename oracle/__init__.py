@@ -68,6 +68,8 @@ def _load():
             I64, I32, P, I64, I64, P, I64, P, I64, P, P, P, P, I64, I64, P, P, F32, F32,
             P, P, P, I64, I32, I32, I32, P, P]
         lib.oracle_qk_prepare_store.restype = ctypes.c_int
+        lib.oracle_qk_prepare_store_chain.argtypes = lib.oracle_qk_prepare_store.argtypes
+        lib.oracle_qk_prepare_store_chain.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -182,10 +184,12 @@ def k_prepare_store(k, k_stride_t, positions, slots, cos_t, sin_t, cs_stride,
 def qk_prepare_store(q, q_stride_t, q_stride_h, k, k_stride_t, w, w_stride_t,
                      positions, slots, cos_t, sin_t, cs_stride, max_position,
                      gamma, beta, eps, softmax_scale, q_fp8, weights, cache,
-                     num_pages, page_size, H, rope_dim, style, T=None):
+                     num_pages, page_size, H, rope_dim, style, T=None, chain=False):
     """Fused Q/K prepare-and-store.  q/k/w are bf16 bit patterns (uint16)
     with the given strides in elements.  ``q_fp8`` ([T, H, 128] uint8),
     ``weights`` ([T, H] fp32) and ``cache`` (uint8) are written in place.
+    ``chain=True`` gives the outputs of the four-launch unfused chain, which
+    rounds the LayerNorm output and the rotated vectors to bf16.
     Returns (err_bits, q_scale_exp[T, H], k_scale_exp[T])."""
     lib = _load()
     positions = _req(positions, np.int64)
@@ -201,7 +205,8 @@ def qk_prepare_store(q, q_stride_t, q_stride_h, k, k_stride_t, w, w_stride_t,
         raise ValueError("output buffers too small")
     qe = np.zeros((max(T, 1), H), np.int32)
     ke = np.zeros(max(T, 1), np.int32)
-    err = lib.oracle_qk_prepare_store(
+    fn = lib.oracle_qk_prepare_store_chain if chain else lib.oracle_qk_prepare_store
+    err = fn(
         T, H, _ptr(q), q_stride_t, q_stride_h, _ptr(k), k_stride_t, _ptr(w), w_stride_t,
         _ptr(positions), _ptr(slots), _ptr(cos_t), _ptr(sin_t), cs_stride, max_position,
         _ptr(gamma), _ptr(beta), eps, softmax_scale, _ptr(q_fp8), _ptr(weights),

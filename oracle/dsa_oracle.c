@@ -178,11 +178,15 @@ static void store_index_k(uint8_t* cache, int64_t slot, int32_t page_size,
   memcpy(page_base + (int64_t)page_size * DSA_D + off * 4, &scale, 4);
 }
 
-/* The k side of one token: bf16 -> fp32, LayerNorm, RoPE, quantise.  With
- * bf16_intermediate the rotated vector is rounded to bf16 just before it is
- * quantised: the unfused writer of [FUSE-QK] Accuracy (note on the two
+/* The k side of one token: bf16 -> fp32, LayerNorm, RoPE, quantise.
+ * bf16_intermediate = 1: the rotated vector is rounded to bf16 just before it
+ * is quantised -- the unfused writer of [FUSE-QK] Accuracy (note on the two
  * writers), which "rounds to bf16 before quantizing"; one rounding there can
- * move a code by at most one step, which is what that note reports. */
+ * move a code by at most one step, which is what that note reports.
+ * bf16_intermediate = 2: the four-launch chain of [FUSE-QK] Profile (rope,
+ * LayerNorm, act_quant, k quant + cache as separate kernels), which hands bf16
+ * tensors from launch to launch: the LayerNorm output and the rotated vector
+ * are both rounded to bf16. */
 static int prepare_k(const uint16_t* krow, const float* cos_row,
                      const float* sin_row, const float* gamma,
                      const float* beta, float eps, int rope_dim, int style,
@@ -190,6 +194,8 @@ static int prepare_k(const uint16_t* krow, const float* cos_row,
   float x[DSA_D], y[DSA_D];
   for (int j = 0; j < DSA_D; ++j) x[j] = bf16_to_f32(krow[j]);
   oracle_layernorm(x, gamma, beta, eps, y);
+  if (bf16_intermediate == 2)
+    for (int j = 0; j < DSA_D; ++j) y[j] = round_to_bf16(y[j]);
   oracle_rope(y, cos_row, sin_row, rope_dim, style);
   if (bf16_intermediate)
     for (int j = 0; j < DSA_D; ++j) y[j] = round_to_bf16(y[j]);
@@ -231,12 +237,9 @@ int oracle_k_prepare_store(int64_t T, const uint16_t* k, int64_t k_stride_t,
   return err;
 }
 
-/* The fused Q/K prepare-and-store ([FUSE-QK] Motivation and Modifications:
- * one call returns (q_fp8, weights) and writes the index-K cache; [FUSE-Q]
- * Summary: RoPE + FP8 quantization + weight-scale fold on the q side).
- * q_fp8 is [T, H, 128] e4m3 codes, weights is [T, H] fp32:
- *   weights[t, h] = w[t, h] * 2^e_q[t, h] * softmax_scale * H^-0.5. */
-int oracle_qk_prepare_store(
+/* Both Q/K writers; chain != 0 rounds the tensors the four-launch chain
+ * hands between launches to bf16 (see prepare_k). */
+static int qk_prepare_store(
     int64_t T, int32_t H, const uint16_t* q, int64_t q_stride_t,
     int64_t q_stride_h, const uint16_t* k, int64_t k_stride_t,
     const uint16_t* w, int64_t w_stride_t, const int64_t* positions,
@@ -245,7 +248,7 @@ int oracle_qk_prepare_store(
     const float* beta, float eps, float softmax_scale, uint8_t* q_fp8,
     float* weights, uint8_t* cache, int64_t num_pages, int32_t page_size,
     int32_t rope_dim, int32_t style, int32_t* q_scale_exp,
-    int32_t* k_scale_exp) {
+    int32_t* k_scale_exp, int chain) {
   int err = 0;
   double head_factor = 1.0 / sqrt((double)H);
   for (int64_t t = 0; t < T; ++t) {
@@ -261,6 +264,8 @@ int oracle_qk_prepare_store(
       float z[DSA_D];
       for (int j = 0; j < DSA_D; ++j) z[j] = bf16_to_f32(qrow[j]);
       oracle_rope(z, cos_row, sin_row, rope_dim, style);
+      if (chain)
+        for (int j = 0; j < DSA_D; ++j) z[j] = round_to_bf16(z[j]);
       int e = oracle_quantize_vector(z, q_fp8 + (t * H + h) * DSA_D);
       if (q_scale_exp) q_scale_exp[t * H + h] = e;
       double wv = (double)bf16_to_f32(w[t * w_stride_t + h]);
@@ -271,7 +276,49 @@ int oracle_qk_prepare_store(
                                   positions + t, slots + t, cos_t, sin_t,
                                   cs_stride, max_position, gamma, beta, eps,
                                   cache, num_pages, page_size, rope_dim, style,
-                                  0, k_scale_exp ? k_scale_exp + t : NULL);
+                                  chain ? 2 : 0, k_scale_exp ? k_scale_exp + t : NULL);
   }
   return err;
+}
+
+/* The fused Q/K prepare-and-store ([FUSE-QK] Motivation and Modifications:
+ * one call returns (q_fp8, weights) and writes the index-K cache; [FUSE-Q]
+ * Summary: RoPE + FP8 quantization + weight-scale fold on the q side).
+ * q_fp8 is [T, H, 128] e4m3 codes, weights is [T, H] fp32:
+ *   weights[t, h] = w[t, h] * 2^e_q[t, h] * softmax_scale * H^-0.5. */
+int oracle_qk_prepare_store(
+    int64_t T, int32_t H, const uint16_t* q, int64_t q_stride_t,
+    int64_t q_stride_h, const uint16_t* k, int64_t k_stride_t,
+    const uint16_t* w, int64_t w_stride_t, const int64_t* positions,
+    const int64_t* slots, const float* cos_t, const float* sin_t,
+    int64_t cs_stride, int64_t max_position, const float* gamma,
+    const float* beta, float eps, float softmax_scale, uint8_t* q_fp8,
+    float* weights, uint8_t* cache, int64_t num_pages, int32_t page_size,
+    int32_t rope_dim, int32_t style, int32_t* q_scale_exp,
+    int32_t* k_scale_exp) {
+  return qk_prepare_store(T, H, q, q_stride_t, q_stride_h, k, k_stride_t, w,
+                          w_stride_t, positions, slots, cos_t, sin_t, cs_stride,
+                          max_position, gamma, beta, eps, softmax_scale, q_fp8,
+                          weights, cache, num_pages, page_size, rope_dim, style,
+                          q_scale_exp, k_scale_exp, 0);
+}
+
+/* The same outputs as written by the four-launch chain of [FUSE-QK] Profile,
+ * whose launches pass bf16 tensors: the key's LayerNorm output and every
+ * rotated vector (q and k) are rounded to bf16 before the next step. */
+int oracle_qk_prepare_store_chain(
+    int64_t T, int32_t H, const uint16_t* q, int64_t q_stride_t,
+    int64_t q_stride_h, const uint16_t* k, int64_t k_stride_t,
+    const uint16_t* w, int64_t w_stride_t, const int64_t* positions,
+    const int64_t* slots, const float* cos_t, const float* sin_t,
+    int64_t cs_stride, int64_t max_position, const float* gamma,
+    const float* beta, float eps, float softmax_scale, uint8_t* q_fp8,
+    float* weights, uint8_t* cache, int64_t num_pages, int32_t page_size,
+    int32_t rope_dim, int32_t style, int32_t* q_scale_exp,
+    int32_t* k_scale_exp) {
+  return qk_prepare_store(T, H, q, q_stride_t, q_stride_h, k, k_stride_t, w,
+                          w_stride_t, positions, slots, cos_t, sin_t, cs_stride,
+                          max_position, gamma, beta, eps, softmax_scale, q_fp8,
+                          weights, cache, num_pages, page_size, rope_dim, style,
+                          q_scale_exp, k_scale_exp, 1);
 }

@@ -26,6 +26,7 @@ __all__ = [
     "DsaError", "NEOX", "GPTJ", "HEAD_DIM", "DEVERR_POSITION", "DEVERR_SLOT", "DEVERR_TIMEOUT",
     "FLAG_PDL", "FLAG_PIPELINE", "FLAG_DIRECT", "FLAG_PDL_EARLY_ROPE",
     "dsa_indexer_qk_prepare_store", "dsa_indexer_k_prepare_store", "dsa_status_string",
+    "dsa_indexer_qk_prepare_store_unfused", "dsa_unfused_workspace_bytes",
     "library", "cache_bytes", "cache_views",
 ]
 
@@ -67,6 +68,13 @@ def library() -> ctypes.CDLL:
         lib.dsa_indexer_k_prepare_store.argtypes = [
             P, I64, P, P, P, P, I64, I64, P, P, F32, P, I64, I32, I32, I32, I32, I32, U32, P, P]
         lib.dsa_indexer_k_prepare_store.restype = ctypes.c_int
+        SZ = ctypes.c_size_t
+        lib.dsa_unfused_workspace_bytes.argtypes = [I32, I32]
+        lib.dsa_unfused_workspace_bytes.restype = SZ
+        lib.dsa_indexer_qk_prepare_store_unfused.argtypes = [
+            P, I64, I64, P, I64, P, I64, P, P, P, P, I64, I64, P, P, F32, F32, P, P, P, I64, I32,
+            I32, I32, I32, I32, I32, U32, P, SZ, P, P]
+        lib.dsa_indexer_qk_prepare_store_unfused.restype = ctypes.c_int
         lib.dsa_status_string.argtypes = [ctypes.c_int]
         lib.dsa_status_string.restype = ctypes.c_char_p
         lib.dsa_prep_version.argtypes = []
@@ -159,26 +167,11 @@ def _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_be
     return 0, 1 << 62
 
 
-def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, sin_cache,
-                                 ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
-                                 page_size, rope_dim=64, rope_style=NEOX, *, q_fp8_out=None,
-                                 weights_out=None, err_flags=None, num_tokens=None,
-                                 max_position=None, pdl=False, kernel="auto", stream=None):
-    """Fused Q/K prepare-and-store (one kernel launch).
-
-    q [T, H, 128] bf16, k [T, 128] bf16, w [T, H] bf16 (row strides of any
-    view are honoured), positions/out_cache_loc [T] int64, cos/sin caches
-    [max_position, >= rope_dim/2] fp32, ln_gamma/ln_beta [128] fp32,
-    index_k_cache: a contiguous CUDA buffer of whole pages (written in place).
-    ``num_tokens`` limits the call to the first T live tokens (the graph
-    split-op contract); outputs are sized to it.  ``pdl`` launches with
-    programmatic dependent launch (the kernel may start while the previous
-    kernel of the stream drains; it still waits for that kernel's memory);
-    ``pdl="early"`` also reads positions, slots and cos/sin before that wait
-    (only when the previous kernel does not write them).
-    ``kernel`` = "auto" | "direct" | "pipeline" overrides the size-based
-    choice between the two kernels (same bytes either way).
-    Returns (q_fp8 [T, H, 128] float8_e4m3fn, weights [T, H] fp32)."""
+def _qk_args(q, k, w, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta,
+             ln_eps, softmax_scale, index_k_cache, page_size, rope_dim, rope_style, q_fp8_out,
+             weights_out, num_tokens, max_position):
+    """Checks and the C argument list shared by the fused and unfused calls,
+    up to and including rope_style; also returns the two outputs."""
     _need(q, "q", torch.bfloat16, 3)
     _need(w, "w", torch.bfloat16, 2)
     cs_stride, rows = _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
@@ -203,17 +196,79 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
             or weights_out.numel() < T * H:
         raise ValueError("weights_out must be contiguous fp32 [T, H]")
     max_position = rows if max_position is None else int(max_position)
+    args = (_ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), _ptr(w), w.stride(0),
+            _ptr(positions), _ptr(out_cache_loc), _ptr(cos_cache) if rope_dim else None,
+            _ptr(sin_cache) if rope_dim else None, cs_stride, max_position, _ptr(ln_gamma),
+            _ptr(ln_beta), float(ln_eps), float(softmax_scale), _ptr(q_fp8_out),
+            _ptr(weights_out), _ptr(index_k_cache), _num_pages(index_k_cache, page_size),
+            page_size, T, H, HEAD_DIM, rope_dim, int(rope_style))
+    outs = (q_fp8_out[:T] if q_fp8_out.dim() == 3 else q_fp8_out,
+            weights_out[:T] if weights_out.dim() == 2 else weights_out)
+    return args, outs, T, H
+
+
+def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, sin_cache,
+                                 ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
+                                 page_size, rope_dim=64, rope_style=NEOX, *, q_fp8_out=None,
+                                 weights_out=None, err_flags=None, num_tokens=None,
+                                 max_position=None, pdl=False, kernel="auto", stream=None):
+    """Fused Q/K prepare-and-store (one kernel launch).
+
+    q [T, H, 128] bf16, k [T, 128] bf16, w [T, H] bf16 (row strides of any
+    view are honoured), positions/out_cache_loc [T] int64, cos/sin caches
+    [max_position, >= rope_dim/2] fp32, ln_gamma/ln_beta [128] fp32,
+    index_k_cache: a contiguous CUDA buffer of whole pages (written in place).
+    ``num_tokens`` limits the call to the first T live tokens (the graph
+    split-op contract); outputs are sized to it.  ``pdl`` launches with
+    programmatic dependent launch (the kernel may start while the previous
+    kernel of the stream drains; it still waits for that kernel's memory);
+    ``pdl="early"`` also reads positions, slots and cos/sin before that wait
+    (only when the previous kernel does not write them).
+    ``kernel`` = "auto" | "direct" | "pipeline" overrides the size-based
+    choice between the two kernels (same bytes either way).
+    Returns (q_fp8 [T, H, 128] float8_e4m3fn, weights [T, H] fp32)."""
+    args, outs, _, _ = _qk_args(q, k, w, positions, out_cache_loc, cos_cache, sin_cache,
+                                ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
+                                page_size, rope_dim, rope_style, q_fp8_out, weights_out,
+                                num_tokens, max_position)
     st = library().dsa_indexer_qk_prepare_store(
-        _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), _ptr(w), w.stride(0),
-        _ptr(positions), _ptr(out_cache_loc), _ptr(cos_cache) if rope_dim else None,
-        _ptr(sin_cache) if rope_dim else None, cs_stride, max_position, _ptr(ln_gamma),
-        _ptr(ln_beta), float(ln_eps), float(softmax_scale), _ptr(q_fp8_out), _ptr(weights_out),
-        _ptr(index_k_cache), _num_pages(index_k_cache, page_size), page_size, T, H, HEAD_DIM,
-        rope_dim, int(rope_style), _flags(pdl, kernel), _ptr(err_flags), _stream(stream))
+        *args, _flags(pdl, kernel), _ptr(err_flags), _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store")
-    return q_fp8_out[:T] if q_fp8_out.dim() == 3 else q_fp8_out, \
-        weights_out[:T] if weights_out.dim() == 2 else weights_out
+    return outs
+
+
+def dsa_unfused_workspace_bytes(T: int, H: int) -> int:
+    """Workspace the unfused chain needs (bf16 intermediates)."""
+    return int(library().dsa_unfused_workspace_bytes(int(T), int(H)))
+
+
+def dsa_indexer_qk_prepare_store_unfused(q, k, w, positions, out_cache_loc, cos_cache,
+                                         sin_cache, ln_gamma, ln_beta, ln_eps, softmax_scale,
+                                         index_k_cache, page_size, rope_dim=64,
+                                         rope_style=NEOX, *, q_fp8_out=None, weights_out=None,
+                                         workspace=None, err_flags=None, num_tokens=None,
+                                         max_position=None, pdl=False, stream=None):
+    """The same computation as four launches (LayerNorm, RoPE, q quant + fold,
+    k quant + store) with bf16 intermediates in ``workspace`` (a CUDA uint8
+    tensor of at least dsa_unfused_workspace_bytes(T, H) bytes; allocated here
+    when not given).  The baseline the fused call is measured against."""
+    args, outs, T, H = _qk_args(q, k, w, positions, out_cache_loc, cos_cache, sin_cache,
+                                ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
+                                page_size, rope_dim, rope_style, q_fp8_out, weights_out,
+                                num_tokens, max_position)
+    need = dsa_unfused_workspace_bytes(T, H)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    st = library().dsa_indexer_qk_prepare_store_unfused(
+        *args, FLAG_PDL if pdl else 0, _ptr(workspace), nbytes, _ptr(err_flags),
+        _stream(stream))
+    if st != 0:
+        raise DsaError(st, "dsa_indexer_qk_prepare_store_unfused")
+    return outs
 
 
 def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,

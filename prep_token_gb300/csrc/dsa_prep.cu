@@ -38,12 +38,12 @@
 #include <cstdint>
 #include <mutex>
 
+#include "dsa_common.cuh"
 #include "dsa_prep.h"
 
 namespace {
 
-constexpr int kD = DSA_HEAD_DIM;
-constexpr unsigned kFull = 0xffffffffu;
+using namespace dsa_dev;
 
 // ---------------------------------------------------------------- parameters
 
@@ -88,416 +88,6 @@ struct Params {
   int* err;
 };
 
-// ---------------------------------------------------------------- PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
-               ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// One bounded probe: the thread may sleep up to ~1 ms inside it, waking as soon
-// as the phase completes, so waiting warps do not spin on issue slots.
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(bar), "r"(parity), "r"(1000000) : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-
-// Wait for the phase with the given parity to complete.  Returns false when
-// the CTA was told to abort or after kWaitLimitNs.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
-                                            volatile int* abort_flag) {
-  const unsigned long long t0 = global_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort_flag);
-}
-
-// Global -> shared bulk copy; completion is counted in bytes on `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
-
-// Programmatic dependent launch: no-ops unless the launch carries the attribute.
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ float pow2f(int e) {
-  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// ---------------------------------------------------------------- memory spaces
-
-// Loads of 2/4/8/16 bytes at a byte address, from global (read-only path,
-// streaming) or from shared memory.
-struct GlobalMem {
-  using Addr = const unsigned char*;
-  __device__ __forceinline__ static uint4 ld16(Addr a) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(a));
-    return r;
-  }
-  __device__ __forceinline__ static uint2 ld8(Addr a) {
-    uint2 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(a));
-    return r;
-  }
-  __device__ __forceinline__ static uint32_t ld4(Addr a) {
-    uint32_t r;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(a));
-    return r;
-  }
-  __device__ __forceinline__ static uint32_t ld2(Addr a) {
-    uint16_t r;
-    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(a));
-    return r;
-  }
-};
-
-struct SharedMem {
-  using Addr = uint32_t;
-  __device__ __forceinline__ static uint4 ld16(Addr a) {
-    uint4 r;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
-    return r;
-  }
-  __device__ __forceinline__ static uint2 ld8(Addr a) {
-    uint2 r;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
-    return r;
-  }
-  __device__ __forceinline__ static uint32_t ld4(Addr a) {
-    uint32_t r;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(a));
-    return r;
-  }
-  __device__ __forceinline__ static uint32_t ld2(Addr a) {
-    uint16_t r;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(r) : "r"(a));
-    return r;
-  }
-};
-
-__host__ __device__ constexpr int pow2_floor(int x) { return x >= 16 ? 16 : x >= 8 ? 8 : x >= 4 ? 4 : x >= 2 ? 2 : 1; }
-__host__ __device__ constexpr int gcd_pow2(int x) { return x == 0 ? 16 : (x & -x) > 16 ? 16 : (x & -x); }
-
-// `BYTES` bytes at `a` (aligned to ALIGN) as 32-bit words w[]; 2-byte pieces
-// land in the low half of a word.
-template <class M, int BYTES, int ALIGN>
-__device__ __forceinline__ void load_words(typename M::Addr a, uint32_t* w) {
-  constexpr int W = pow2_floor(ALIGN < BYTES ? ALIGN : BYTES);
-#pragma unroll
-  for (int b = 0; b < BYTES; b += W) {
-    if constexpr (W == 16) {
-      const uint4 v = M::ld16(a + b);
-      w[b / 4] = v.x; w[b / 4 + 1] = v.y; w[b / 4 + 2] = v.z; w[b / 4 + 3] = v.w;
-    } else if constexpr (W == 8) {
-      const uint2 v = M::ld8(a + b);
-      w[b / 4] = v.x; w[b / 4 + 1] = v.y;
-    } else if constexpr (W == 4) {
-      w[b / 4] = M::ld4(a + b);
-    } else {
-      w[b / 4] = M::ld2(a + b);
-    }
-  }
-}
-
-// N bf16 elements -> fp32 x[0..N)
-template <class M, int N, int ALIGN>
-__device__ __forceinline__ void load_bf16(typename M::Addr a, float* x) {
-  uint32_t w[(2 * N + 3) / 4];
-  load_words<M, 2 * N, ALIGN>(a, w);
-#pragma unroll
-  for (int j = 0; j < N; ++j) x[j] = (j & 1) ? bf16_hi(w[j / 2]) : bf16_lo(w[j / 2]);
-}
-
-// N fp32 values from global (gamma / beta / cos / sin rows), read-only cached.
-template <int N, int ALIGN>
-__device__ __forceinline__ void load_f32_global(const float* p, float* x) {
-  constexpr int W = pow2_floor(ALIGN < 4 * N ? ALIGN : 4 * N);
-#pragma unroll
-  for (int b = 0; b < 4 * N; b += W) {
-    if constexpr (W == 16) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(p + b / 4));
-      x[b / 4] = v.x; x[b / 4 + 1] = v.y; x[b / 4 + 2] = v.z; x[b / 4 + 3] = v.w;
-    } else if constexpr (W == 8) {
-      const float2 v = __ldg(reinterpret_cast<const float2*>(p + b / 4));
-      x[b / 4] = v.x; x[b / 4 + 1] = v.y;
-    } else {
-      x[b / 4] = __ldg(p + b / 4);
-    }
-  }
-}
-
-template <int N, int ALIGN>
-__device__ __forceinline__ void load_f32_shared(uint32_t a, float* x) {
-  uint32_t w[N];
-  load_words<SharedMem, 4 * N, ALIGN>(a, w);
-#pragma unroll
-  for (int j = 0; j < N; ++j) x[j] = __uint_as_float(w[j]);
-}
-
-// Store `BYTES` code bytes (packed little-endian in w[]) at global p.
-template <int BYTES, int ALIGN>
-__device__ __forceinline__ void store_codes(uint8_t* p, const uint32_t* w) {
-  constexpr int W = pow2_floor(ALIGN < BYTES ? ALIGN : BYTES);
-#pragma unroll
-  for (int b = 0; b < BYTES; b += W) {
-    if constexpr (W == 16) {
-      asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p + b), "r"(w[b / 4]),
-                   "r"(w[b / 4 + 1]), "r"(w[b / 4 + 2]), "r"(w[b / 4 + 3]) : "memory");
-    } else if constexpr (W == 8) {
-      asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p + b), "r"(w[b / 4]),
-                   "r"(w[b / 4 + 1]) : "memory");
-    } else if constexpr (W == 4) {
-      asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p + b), "r"(w[b / 4]) : "memory");
-    } else if constexpr (W == 2) {
-      const uint16_t v = static_cast<uint16_t>(w[b / 4] >> (8 * (b & 3)));
-      asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p + b), "h"(v) : "memory");
-    } else {
-      const uint16_t v = static_cast<uint16_t>((w[b / 4] >> (8 * (b & 3))) & 0xff);
-      asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p + b), "h"(v) : "memory");
-    }
-  }
-}
-
-// ---------------------------------------------------------------- the slice
-
-// Where a lane's 16 elements live (element offsets inside the 128-vector and
-// their alignment in bytes for bf16 / e4m3 / fp32 rows).
-template <int STYLE, int RP>
-struct Slice {
-  static constexpr int R = 16 * RP;      // rope_dim
-  static constexpr int NR = 2 * RP;      // rotated elements per lane
-  static constexpr int NP = 16 - NR;     // pass-through elements per lane
-  static constexpr bool NEOX = STYLE == DSA_ROPE_NEOX;
-  // element offset of each chunk for lane l: base + stride * l
-  static constexpr int A_STRIDE = NEOX ? RP : 2 * RP;  // NeoX a-chunk / GPT-J pair chunk
-  static constexpr int B_BASE = R / 2;                  // NeoX b-chunk
-  static constexpr int P_BASE = R;
-  // alignments (bytes) of the per-lane chunk starts
-  static constexpr int ALIGN_A_BF16 = gcd_pow2(2 * A_STRIDE);
-  static constexpr int ALIGN_B_BF16 = gcd_pow2(2 * RP) < gcd_pow2(2 * B_BASE) ? gcd_pow2(2 * RP)
-                                                                               : gcd_pow2(2 * B_BASE);
-  static constexpr int ALIGN_P_BF16 = gcd_pow2(2 * NP) < gcd_pow2(2 * P_BASE) ? gcd_pow2(2 * NP)
-                                                                               : gcd_pow2(2 * P_BASE);
-  static constexpr int ALIGN_A_U8 = gcd_pow2(A_STRIDE);
-  static constexpr int ALIGN_B_U8 = gcd_pow2(RP) < gcd_pow2(B_BASE) ? gcd_pow2(RP) : gcd_pow2(B_BASE);
-  static constexpr int ALIGN_P_U8 = gcd_pow2(NP) < gcd_pow2(P_BASE) ? gcd_pow2(NP) : gcd_pow2(P_BASE);
-  static constexpr int ALIGN_A_F32 = gcd_pow2(4 * A_STRIDE);
-  static constexpr int ALIGN_B_F32 = gcd_pow2(4 * RP) < gcd_pow2(4 * B_BASE) ? gcd_pow2(4 * RP)
-                                                                               : gcd_pow2(4 * B_BASE);
-  static constexpr int ALIGN_P_F32 = gcd_pow2(4 * NP) < gcd_pow2(4 * P_BASE) ? gcd_pow2(4 * NP)
-                                                                               : gcd_pow2(4 * P_BASE);
-  static constexpr int ALIGN_CS = gcd_pow2(4 * RP);
-};
-
-// Load the lane's 16 bf16 values of a row into x[]: x[0..RP) the a-members,
-// x[RP..2RP) the b-members, x[2RP..16) the pass-through values.
-template <int STYLE, int RP, class M>
-__device__ __forceinline__ void load_slice(typename M::Addr row, int l, float (&x)[16]) {
-  using S = Slice<STYLE, RP>;
-  if constexpr (RP > 0) {
-    if constexpr (S::NEOX) {
-      load_bf16<M, RP, S::ALIGN_A_BF16>(row + 2 * RP * l, x);
-      load_bf16<M, RP, S::ALIGN_B_BF16>(row + 2 * (S::B_BASE + RP * l), x + RP);
-    } else {
-      float t[2 * RP];
-      load_bf16<M, 2 * RP, S::ALIGN_A_BF16>(row + 4 * RP * l, t);
-#pragma unroll
-      for (int j = 0; j < RP; ++j) x[j] = t[2 * j], x[RP + j] = t[2 * j + 1];
-    }
-  }
-  if constexpr (S::NP > 0) load_bf16<M, S::NP, S::ALIGN_P_BF16>(row + 2 * (S::P_BASE + S::NP * l), x + 2 * RP);
-}
-
-// Rotation operands of the lane: frequencies RP*l .. RP*l + RP - 1.
-template <int RP>
-struct Rot {
-  float c[RP > 0 ? RP : 1];
-  float s[RP > 0 ? RP : 1];
-  float ns[RP > 0 ? RP : 1];
-};
-
-template <int RP>
-__device__ __forceinline__ void finish_rot(Rot<RP>& r) {
-#pragma unroll
-  for (int j = 0; j < RP; ++j) r.ns[j] = -r.s[j];
-}
-
-// RoPE on the lane's pairs (a_j, b_j):
-//   a' = fma(a, c, b * (-s)) = fma(a, c, -(b*s)),  b' = fma(b, c, a * s),
-// products rounded to fp32 (no contraction), two pairs per packed instruction.
-template <int RP>
-__device__ __forceinline__ void rope_slice(float (&x)[16], const Rot<RP>& r) {
-  if constexpr (RP == 1) {
-    const float a = x[0], b = x[1];
-    x[0] = __fmaf_rn(a, r.c[0], __fmul_rn(b, r.ns[0]));
-    x[1] = __fmaf_rn(b, r.c[0], __fmul_rn(a, r.s[0]));
-  } else {
-#pragma unroll
-    for (int j = 0; j < RP; j += 2) {
-      const float2 a = make_float2(x[j], x[j + 1]);
-      const float2 b = make_float2(x[RP + j], x[RP + j + 1]);
-      const float2 c = make_float2(r.c[j], r.c[j + 1]);
-      const float2 pa = __fmul2_rn(b, make_float2(r.ns[j], r.ns[j + 1]));
-      const float2 pb = __fmul2_rn(a, make_float2(r.s[j], r.s[j + 1]));
-      const float2 na = __ffma2_rn(a, c, pa);
-      const float2 nb = __ffma2_rn(b, c, pb);
-      x[j] = na.x; x[j + 1] = na.y;
-      x[RP + j] = nb.x; x[RP + j + 1] = nb.y;
-    }
-  }
-}
-
-// Quarter-warp reductions (xor offsets 4, 2, 1 stay inside the 8-lane group).
-__device__ __forceinline__ float quad_max(float v) {
-  v = fmaxf(v, __shfl_xor_sync(kFull, v, 4));
-  v = fmaxf(v, __shfl_xor_sync(kFull, v, 2));
-  v = fmaxf(v, __shfl_xor_sync(kFull, v, 1));
-  return v;
-}
-
-__device__ __forceinline__ float quad_sum(float v) {
-  v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 4));
-  v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 2));
-  v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 1));
-  return v;
-}
-
-// ue8m0 exponent of the vector: the smallest e with max(amax, 1e-4) <= 448*2^e.
-// With A = max(amax, 1e-4) = 1.f * 2^E (normal), 448 * 2^e = 1.75 * 2^(e+8), so
-// e = E - 8 when the fraction is <= 0.75 (bits <= 0x600000) and E - 7 above:
-// read straight off the exponent and fraction bits, no division or log.
-__device__ __forceinline__ int ue8m0_exponent(const float (&x)[16]) {
-  float m = max3f(fabsf(x[0]), fabsf(x[1]), fabsf(x[2]));
-#pragma unroll
-  for (int j = 3; j < 15; j += 2) m = max3f(m, fabsf(x[j]), fabsf(x[j + 1]));
-  m = fmaxf(m, fabsf(x[15]));
-  m = fmaxf(quad_max(m), 1e-4f);
-  const uint32_t b = __float_as_uint(m);
-  return static_cast<int>(b >> 23) - 135 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0);
-}
-
-// e4m3 codes of x * 2^-e (the multiply by a power of two is exact), packed in
-// element order of each chunk: words wa (a-chunk or GPT-J pair chunk), wb
-// (NeoX b-chunk), wp (pass-through chunk).
-template <int STYLE, int RP>
-__device__ __forceinline__ void quantize_slice(const float (&x)[16], int e, uint32_t* wa,
-                                               uint32_t* wb, uint32_t* wp) {
-  using S = Slice<STYLE, RP>;
-  const float inv = pow2f(-e);
-  const float2 i2 = make_float2(inv, inv);
-  float v[16];
-#pragma unroll
-  for (int j = 0; j < 16; j += 2) {
-    const float2 t = __fmul2_rn(make_float2(x[j], x[j + 1]), i2);
-    v[j] = t.x;
-    v[j + 1] = t.y;
-  }
-  if constexpr (RP > 0) {
-    if constexpr (S::NEOX) {
-      // a-chunk: v[0..RP), b-chunk: v[RP..2RP); RP = 1 packs a lone code
-#pragma unroll
-      for (int j = 0; j < RP; j += 2) {
-        const uint32_t ca = cvt_e4m3x2(v[j], RP > 1 ? v[j + 1] : 0.0f);
-        const uint32_t cb = cvt_e4m3x2(v[RP + j], RP > 1 ? v[RP + j + 1] : 0.0f);
-        if ((j & 2) == 0) wa[j / 4] = ca, wb[j / 4] = cb;
-        else wa[j / 4] |= ca << 16, wb[j / 4] |= cb << 16;
-      }
-    } else {
-      // pair chunk in element order: a_0 b_0 a_1 b_1 ...
-#pragma unroll
-      for (int j = 0; j < RP; ++j) {
-        const uint32_t c = cvt_e4m3x2(v[j], v[RP + j]);
-        if ((j & 1) == 0) wa[j / 2] = c;
-        else wa[j / 2] |= c << 16;
-      }
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < S::NP; j += 2) {
-    const uint32_t c = cvt_e4m3x2(v[2 * RP + j], v[2 * RP + j + 1]);
-    if ((j & 2) == 0) wp[j / 4] = c;
-    else wp[j / 4] |= c << 16;
-  }
-}
-
-template <int STYLE, int RP>
-__device__ __forceinline__ void store_slice(uint8_t* row, int l, const uint32_t* wa,
-                                            const uint32_t* wb, const uint32_t* wp) {
-  using S = Slice<STYLE, RP>;
-  if constexpr (RP > 0) {
-    if constexpr (S::NEOX) {
-      store_codes<RP, S::ALIGN_A_U8>(row + RP * l, wa);
-      store_codes<RP, S::ALIGN_B_U8>(row + S::B_BASE + RP * l, wb);
-    } else {
-      store_codes<2 * RP, S::ALIGN_A_U8>(row + 2 * RP * l, wa);
-    }
-  }
-  if constexpr (S::NP > 0) store_codes<S::NP, S::ALIGN_P_U8>(row + S::P_BASE + S::NP * l, wp);
-}
-
 // Query vector: rotate, quantise, store codes; returns the scale exponent.
 template <int STYLE, int RP>
 __device__ __forceinline__ int q_slice(float (&x)[16], const Rot<RP>& r, uint8_t* out_row,
@@ -516,50 +106,6 @@ __device__ __forceinline__ void raise_error(const Params& p, int bit) {
 
 // Key vector: LayerNorm (mean, biased variance, eps inside the root), RoPE,
 // quantise, and store the codes and the scale into slot `slot` of the cache.
-// y = x * rstd * gamma + beta on n values whose gamma/beta start at `row`
-// (fp32 [128] rows), one aligned piece at a time to keep few registers live.
-template <int N, int ALIGN>
-__device__ __forceinline__ void affine_piece(const float* g_row, const float* b_row, float* x,
-                                             float rstd) {
-  float g[N], b[N];
-  load_f32_global<N, ALIGN>(g_row, g);
-  load_f32_global<N, ALIGN>(b_row, b);
-#pragma unroll
-  for (int j = 0; j < N; ++j) x[j] = __fmaf_rn(__fmul_rn(x[j], rstd), g[j], b[j]);
-}
-
-template <int STYLE, int RP>
-__device__ __forceinline__ void affine_slice(const Params& p, int l, float (&x)[16], float rstd) {
-  using S = Slice<STYLE, RP>;
-  if constexpr (RP > 0) {
-    if constexpr (S::NEOX) {
-      affine_piece<RP, S::ALIGN_A_F32>(p.gamma + RP * l, p.beta + RP * l, x, rstd);
-      affine_piece<RP, S::ALIGN_B_F32>(p.gamma + S::B_BASE + RP * l, p.beta + S::B_BASE + RP * l,
-                                       x + RP, rstd);
-    } else {
-      float g[2 * RP], b[2 * RP];
-      load_f32_global<2 * RP, S::ALIGN_A_F32>(p.gamma + 2 * RP * l, g);
-      load_f32_global<2 * RP, S::ALIGN_A_F32>(p.beta + 2 * RP * l, b);
-#pragma unroll
-      for (int j = 0; j < RP; ++j) {
-        x[j] = __fmaf_rn(__fmul_rn(x[j], rstd), g[2 * j], b[2 * j]);
-        x[RP + j] = __fmaf_rn(__fmul_rn(x[RP + j], rstd), g[2 * j + 1], b[2 * j + 1]);
-      }
-    }
-  }
-  constexpr int NP = S::NP;
-  if constexpr (NP > 0) {
-    // pieces of at most 4 values
-    constexpr int PIECE = NP >= 4 ? 4 : NP;
-#pragma unroll
-    for (int j = 0; j < NP; j += PIECE) {
-      constexpr int A = S::ALIGN_P_F32 < 4 * PIECE ? S::ALIGN_P_F32 : 4 * PIECE;
-      affine_piece<PIECE, A>(p.gamma + S::P_BASE + NP * l + j, p.beta + S::P_BASE + NP * l + j,
-                             x + 2 * RP + j, rstd);
-    }
-  }
-}
-
 template <int STYLE, int RP>
 __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const Rot<RP>& r,
                                         int l, bool real, bool pos_ok, long long slot) {
@@ -575,7 +121,7 @@ __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const R
   }
   const float var = __fmul_rn(quad_sum(sq), 1.0f / kD);
   const float rstd = __frsqrt_rn(__fadd_rn(var, p.eps));
-  affine_slice<STYLE, RP>(p, l, x, rstd);
+  affine_slice<STYLE, RP>(p.gamma, p.beta, l, x, rstd);
   if constexpr (RP > 0) rope_slice<RP>(x, r);
   const int e = ue8m0_exponent(x);
   uint32_t wa[4], wb[4], wp[4];

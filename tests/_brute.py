@@ -54,9 +54,18 @@ def quant64(z):
     return codes, e
 
 
-def pipeline(inp, H=None):
+def bf16_round(v):
+    """float64 values -> nearest bf16 (ties to even), as float64."""
+    v = np.asarray(v, np.float64)
+    m, e = np.frexp(v)                    # v = m * 2^e, |m| in [0.5, 1)
+    q = np.round(m * 256.0)               # 8 significant bits; np.round is ties-to-even
+    return np.ldexp(q / 256.0, e)
+
+
+def pipeline(inp, H=None, chain=False):
     """Returns (q_codes[T,H,128], q_exp[T,H], weights[T,H], k_codes[T,128],
-    k_exp[T]) in float64 arithmetic."""
+    k_exp[T]) in float64 arithmetic.  chain=True rounds the LayerNorm output
+    and the rotated vectors to bf16, as the four-launch chain does."""
     T = inp.T
     H = inp.H if H is None else H
     kb = inp.k_buffer().reshape(-1)
@@ -73,6 +82,8 @@ def pipeline(inp, H=None):
         for h in range(H):
             x = bf16(inp.q[t, h])
             z = rope64(x, c, s, inp.rope_dim, inp.style)
+            if chain:
+                z = bf16_round(z)
             qc[t, h], qe[t, h] = quant64(z)
             wv = bf16(wb[t * inp.w_stride_t + w_off + h])
             wt[t, h] = wv * 2.0 ** qe[t, h] * float(np.float32(inp.softmax_scale)) / np.sqrt(H)
@@ -80,6 +91,10 @@ def pipeline(inp, H=None):
         mu = x.mean()
         var = ((x - mu) ** 2).mean()
         y = (x - mu) / np.sqrt(var + float(np.float32(inp.eps))) * inp.gamma + inp.beta
+        if chain:
+            y = bf16_round(y)
         z = rope64(y, c, s, inp.rope_dim, inp.style)
+        if chain:
+            z = bf16_round(z)
         kc[t], ke[t] = quant64(z)
     return qc, qe, wt, kc, ke

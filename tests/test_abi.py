@@ -100,3 +100,32 @@ def test_binding_rejects_cpu_tensors(lib):
     with pytest.raises(ValueError, match="CUDA"):
         dp.dsa_indexer_qk_prepare_store(q, q[:, 0], q[:, :, 0], None, None, None, None, None,
                                         None, 1e-6, 0.1, None, 64)
+
+
+def _unf(lib, **over):
+    args = dict(q=A, sqt=64 * 128, sqh=128, k=A, skt=128, w=A, swt=64, pos=A, loc=A, cos=A,
+                sin=A, cs=32, maxpos=4096, g=A, b=A, eps=1e-6, sm=0.088, qo=A, wo=A, cache=A,
+                pages=4, ps=64, T=4, H=64, D=128, r=64, style=0, flags=0, ws=0x100000,
+                wsb=1 << 20, err=None, stream=None)
+    args.update(over)
+    return lib.dsa_indexer_qk_prepare_store_unfused(*args.values())
+
+
+def test_unfused_workspace_size(lib):
+    assert lib.dsa_unfused_workspace_bytes(4, 64) == 2 * 1024 + 4 * 64 * 256
+    assert lib.dsa_unfused_workspace_bytes(3, 5) == 2 * 768 + 3 * 5 * 256
+    assert lib.dsa_unfused_workspace_bytes(-1, 5) == 0
+    assert lib.dsa_unfused_workspace_bytes(4, 0) == 0
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(T=-1), 3), (dict(H=0), 3), (dict(D=64), 4), (dict(r=48), 4), (dict(style=3), 4),
+    (dict(flags=2), 4), (dict(ws=None), 1), (dict(wsb=1000), 3), (dict(ws=0x100000 + 16), 2),
+    (dict(q=A + 2), 2), (dict(cache=None), 1), (dict(ps=6), 2), (dict(swt=8), 3),
+])
+def test_unfused_validation(lib, over, status):
+    assert _unf(lib, **over) == status
+
+
+def test_unfused_empty_batch(lib):
+    assert _unf(lib, T=0, q=None, k=None, ws=None, wsb=0) == 0
