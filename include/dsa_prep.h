@@ -77,7 +77,9 @@ typedef enum {
   DSA_ERR_ALIGN = 2,       /* a pointer or stride breaks an alignment rule */
   DSA_ERR_SHAPE = 3,       /* a negative or inconsistent size or stride */
   DSA_ERR_UNSUPPORTED = 4, /* head_dim != 128, bad rope_dim, style or flag */
-  DSA_ERR_LAUNCH = 5       /* the CUDA launch itself failed */
+  DSA_ERR_LAUNCH = 5,      /* the CUDA launch itself failed */
+  DSA_ERR_SCRATCH_LIMIT = 6 /* the call needs more than the library's built-in
+                               scratch buffer holds (the _noalloc entry point) */
 } dsa_status;
 
 typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
@@ -198,6 +200,47 @@ dsa_status dsa_indexer_qk_prepare_store_unfused(
     int32_t T, int32_t H, int32_t head_dim, int32_t rope_dim,
     int32_t rope_style, uint32_t flags, void* workspace, size_t workspace_bytes,
     int32_t* err_flags, void* stream);
+
+/*
+ * The unfused chain without a caller workspace, for callers that cannot
+ * allocate device memory when they run it: an engine that gives the whole GPU
+ * to its own memory pool at start-up and forbids other allocations, a plugin
+ * host that only hands over pointers to inputs and outputs, or code in a
+ * place where cudaMalloc would synchronise or is not allowed.  The paper has
+ * no counterpart to this entry point; it is an interface convenience.
+ *
+ * The bf16 intermediates go to a 32 MiB buffer compiled into the library (a
+ * fixed array in device global memory, present on every GPU that loads the
+ * library until the process exits).  A call therefore needs
+ * dsa_unfused_workspace_bytes(T, H) <= 32 MiB, i.e. T * (H + 2) <= 131072;
+ * larger calls return DSA_ERR_SCRATCH_LIMIT and launch nothing.
+ *
+ * The caller still passes all inputs and outputs; the call allocates nothing
+ * (no cudaMalloc or cudaFree).  The first call on each device looks the
+ * buffer's device address up once, with that device current -- make that
+ * first call outside any stream capture.
+ *
+ * All calls on a device share the one buffer: two calls that may run on the
+ * GPU at the same time (different streams without ordering between them)
+ * race and corrupt each other's results.  Order them (one stream, or events).
+ * The buffer keeps whatever the last call left in it; the chain writes every
+ * intermediate before reading it, so nothing needs clearing between calls.
+ * Arguments, checks and results are otherwise those of
+ * dsa_indexer_qk_prepare_store_unfused.
+ */
+dsa_status dsa_indexer_qk_prepare_store_unfused_noalloc(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    const void* k, int64_t k_stride_t,
+    const void* w, int64_t w_stride_t,
+    const int64_t* positions, const int64_t* out_cache_loc,
+    const float* cos_cache, const float* sin_cache, int64_t cs_stride,
+    int64_t max_position,
+    const float* ln_gamma, const float* ln_beta, float ln_eps,
+    float softmax_scale,
+    void* q_fp8_out, float* weights_out,
+    void* index_k_cache, int64_t num_pages, int32_t page_size,
+    int32_t T, int32_t H, int32_t head_dim, int32_t rope_dim,
+    int32_t rope_style, uint32_t flags, int32_t* err_flags, void* stream);
 
 /* A static, NUL-terminated description of a status code. */
 const char* dsa_status_string(dsa_status status);

@@ -27,6 +27,7 @@ __all__ = [
     "FLAG_PDL", "FLAG_PIPELINE", "FLAG_DIRECT", "FLAG_PDL_EARLY_ROPE",
     "dsa_indexer_qk_prepare_store", "dsa_indexer_k_prepare_store", "dsa_status_string",
     "dsa_indexer_qk_prepare_store_unfused", "dsa_unfused_workspace_bytes",
+    "dsa_indexer_qk_prepare_store_unfused_noalloc",
     "library", "cache_bytes", "cache_views",
 ]
 
@@ -38,7 +39,7 @@ _KERNEL_FLAGS = {"auto": 0, "pipeline": FLAG_PIPELINE, "direct": FLAG_DIRECT}
 ROW_BYTES = HEAD_DIM + 4  # 128 codes + one fp32 scale per slot
 
 _STATUS = {0: "DSA_OK", 1: "DSA_ERR_NULL", 2: "DSA_ERR_ALIGN", 3: "DSA_ERR_SHAPE",
-           4: "DSA_ERR_UNSUPPORTED", 5: "DSA_ERR_LAUNCH"}
+           4: "DSA_ERR_UNSUPPORTED", 5: "DSA_ERR_LAUNCH", 6: "DSA_ERR_SCRATCH_LIMIT"}
 
 
 class DsaError(RuntimeError):
@@ -75,6 +76,10 @@ def library() -> ctypes.CDLL:
             P, I64, I64, P, I64, P, I64, P, P, P, P, I64, I64, P, P, F32, F32, P, P, P, I64, I32,
             I32, I32, I32, I32, I32, U32, P, SZ, P, P]
         lib.dsa_indexer_qk_prepare_store_unfused.restype = ctypes.c_int
+        lib.dsa_indexer_qk_prepare_store_unfused_noalloc.argtypes = [
+            P, I64, I64, P, I64, P, I64, P, P, P, P, I64, I64, P, P, F32, F32, P, P, P, I64, I32,
+            I32, I32, I32, I32, I32, U32, P, P]
+        lib.dsa_indexer_qk_prepare_store_unfused_noalloc.restype = ctypes.c_int
         lib.dsa_status_string.argtypes = [ctypes.c_int]
         lib.dsa_status_string.restype = ctypes.c_char_p
         lib.dsa_prep_version.argtypes = []
@@ -268,6 +273,32 @@ def dsa_indexer_qk_prepare_store_unfused(q, k, w, positions, out_cache_loc, cos_
         _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store_unfused")
+    return outs
+
+
+def dsa_indexer_qk_prepare_store_unfused_noalloc(q, k, w, positions, out_cache_loc, cos_cache,
+                                                 sin_cache, ln_gamma, ln_beta, ln_eps,
+                                                 softmax_scale, index_k_cache, page_size,
+                                                 rope_dim=64, rope_style=NEOX, *, q_fp8_out,
+                                                 weights_out, err_flags=None, num_tokens=None,
+                                                 max_position=None, pdl=False, stream=None):
+    """The unfused chain with its intermediates in the library's own 32 MiB
+    device buffer, for callers that cannot allocate device memory when they
+    run it (an engine whose memory pool owns the whole GPU, a plugin handed
+    only input and output pointers).  Nothing is allocated here either: the
+    caller passes q_fp8_out and weights_out.  Calls that overlap on the GPU
+    share the buffer and race; calls with T * (H + 2) * 256 bytes of
+    intermediates above 32 MiB raise DsaError (DSA_ERR_SCRATCH_LIMIT)."""
+    if q_fp8_out is None or weights_out is None:
+        raise ValueError("pass q_fp8_out and weights_out: this entry point allocates nothing")
+    args, outs, _, _ = _qk_args(q, k, w, positions, out_cache_loc, cos_cache, sin_cache,
+                                ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
+                                page_size, rope_dim, rope_style, q_fp8_out, weights_out,
+                                num_tokens, max_position)
+    st = library().dsa_indexer_qk_prepare_store_unfused_noalloc(
+        *args, FLAG_PDL if pdl else 0, _ptr(err_flags), _stream(stream))
+    if st != 0:
+        raise DsaError(st, "dsa_indexer_qk_prepare_store_unfused_noalloc")
     return outs
 
 

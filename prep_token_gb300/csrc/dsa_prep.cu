@@ -695,6 +695,8 @@ const char* dsa_status_string(dsa_status status) {
     case DSA_ERR_SHAPE: return "a negative or inconsistent size or stride";
     case DSA_ERR_UNSUPPORTED: return "unsupported head_dim, rope_dim, rope_style, flag or scalar";
     case DSA_ERR_LAUNCH: return "the CUDA kernel launch failed";
+    case DSA_ERR_SCRATCH_LIMIT:
+      return "the call needs more scratch than the library's built-in 32 MiB buffer";
   }
   return "unknown status";
 }

@@ -14,6 +14,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "dsa_common.cuh"
 #include "dsa_prep.h"
@@ -369,6 +370,76 @@ dsa_status dsa_indexer_qk_prepare_store_unfused(
   if (e == cudaSuccess) e = launch_one(unfused_q_quant_kernel, nq, p, pdl, s);
   if (e == cudaSuccess) e = launch_one(unfused_k_quant_store_kernel, T, p, pdl, s);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_LAUNCH;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation variant
+//
+// Some callers cannot allocate device memory at the moment they run this
+// chain: an engine that hands the whole GPU to its own pool at start-up and
+// forbids any other allocation, a plugin host that only passes the plugin
+// pointers to its inputs and outputs, or code running where a cudaMalloc
+// would synchronise the device or fail (inside a region that is being
+// captured, for example).  For them the chain can use a scratch buffer that
+// lives inside the library itself: a fixed array in device global memory,
+// created when the library's device code is loaded on a GPU and kept until
+// the process exits.  Its size caps the call: T * (H + 2) * 256 bytes of
+// intermediates must fit in it.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB per GPU
+
+// Device memory; on the host this name is only a stand-in for the symbol, so
+// the kernels get the address that cudaGetSymbolAddress returns below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+void* g_noalloc_ptr[kMaxScratchDevices] = {};
+std::mutex g_noalloc_mu;
+
+// The scratch array's device address on the current device, looked up once
+// per device (the first call on a device does it, with that device current).
+cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+dsa_status dsa_indexer_qk_prepare_store_unfused_noalloc(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k, int64_t k_stride_t,
+    const void* w, int64_t w_stride_t, const int64_t* positions, const int64_t* out_cache_loc,
+    const float* cos_cache, const float* sin_cache, int64_t cs_stride, int64_t max_position,
+    const float* ln_gamma, const float* ln_beta, float ln_eps, float softmax_scale,
+    void* q_fp8_out, float* weights_out, void* index_k_cache, int64_t num_pages,
+    int32_t page_size, int32_t T, int32_t H, int32_t head_dim, int32_t rope_dim,
+    int32_t rope_style, uint32_t flags, int32_t* err_flags, void* stream) {
+  const size_t need = dsa_unfused_workspace_bytes(T, H);
+  if (T > 0 && need > kNoAllocScratchBytes) return DSA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  if (T > 0 && need > 0 && noalloc_scratch(&scratch) != cudaSuccess) return DSA_ERR_LAUNCH;
+  // Every intermediate the chain reads was written earlier in the same call,
+  // so the buffer's previous contents never matter and nothing is cleared.
+  return dsa_indexer_qk_prepare_store_unfused(
+      q, q_stride_t, q_stride_h, k, k_stride_t, w, w_stride_t, positions, out_cache_loc,
+      cos_cache, sin_cache, cs_stride, max_position, ln_gamma, ln_beta, ln_eps, softmax_scale,
+      q_fp8_out, weights_out, index_k_cache, num_pages, page_size, T, H, head_dim, rope_dim,
+      rope_style, flags, scratch, kNoAllocScratchBytes, err_flags, stream);
 }
 
 }  // extern "C"
