@@ -61,6 +61,17 @@ def _env_int(name, default):
         return default
 
 
+def max_over_ranks(value: float, device="cpu") -> float:
+    """The largest `value` over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -324,11 +335,8 @@ def run_ours(args, rank, world, local_rank):
         stream.synchronize()
     del graphs
     torch.cuda.synchronize(dev)
-    elapsed_ms = e0.elapsed_time(e1)
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
         torch.distributed.barrier()
     ms_per_step = elapsed_ms / args.steps
     value = world * T * args.steps / (elapsed_ms / 1000.0)
@@ -367,11 +375,7 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         f1.record(stream)
     stream.synchronize()
-    e2e_ms = f0.elapsed_time(f1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), dev)
     h2d = h_q.numel() * 2 + h_kw.numel() * 2 + h_pos.numel() * 8 + h_slots.numel() * 8
     d2h = h_qo.numel() + h_wo.numel() * 4
 
