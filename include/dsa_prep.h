@@ -34,7 +34,8 @@
  *
  * Index-K cache layout: num_pages pages of page_size * 132 bytes; page p
  * holds page_size rows of 128 e4m3 codes, then page_size fp32 scales.  Slot s
- * is row s % page_size of page s / page_size.
+ * is row s % page_size of page s / page_size.  DSA_FLAG_CACHE_TOKEN_MAJOR
+ * selects the other layout, 132 bytes per slot (codes, then scale).
  *
  * Conventions shared by every call:
  *   - Pointers are DEVICE pointers owned by the caller; the library allocates
@@ -111,6 +112,13 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
  * memory round trips with its tail.  q, k and w are still read only after the
  * wait.  Without DSA_FLAG_PDL this flag is an error. */
 #define DSA_FLAG_PDL_EARLY_ROPE 8u
+/* Index-K cache layout.  Default (page-blocked): page p holds page_size rows
+ * of 128 e4m3 codes, then page_size fp32 scales; slot s is row s % page_size
+ * of page s / page_size, and page_size must be a multiple of 4.  With this
+ * flag (token-major): slot s owns bytes [132*s, 132*s + 132) -- its 128 codes,
+ * then its fp32 scale -- and page_size only sets the slot count
+ * num_pages * page_size.  Same buffer size either way. */
+#define DSA_FLAG_CACHE_TOKEN_MAJOR 16u
 
 /*
  * Fused Q/K prepare-and-store: returns the (q_fp8, weights) contract and
@@ -135,7 +143,7 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
  *   q_fp8_out      e4m3 bytes [T, H, 128], contiguous, 16-byte aligned.
  *   weights_out    fp32 [T, H], contiguous, 4-byte aligned.
  *   index_k_cache  num_pages * page_size * 132 bytes, 16-byte aligned;
- *                  page_size a multiple of 4.
+ *                  page_size a multiple of 4 (page-blocked layout only).
  *   T >= 0, 1 <= H <= 4096, head_dim == 128, rope_dim in {0, 16, 32, 64, 128},
  *   rope_style a dsa_rope_style, flags a set of DSA_FLAG_* bits.
  */
@@ -181,7 +189,8 @@ dsa_status dsa_indexer_k_prepare_store(
  * scratch).  Because LayerNorm and RoPE outputs are rounded to bf16, its codes
  * can differ from the fused call's by one step near rounding boundaries; its
  * scales and slots follow the same rules.  Arguments and checks are those of
- * dsa_indexer_qk_prepare_store; flags may hold DSA_FLAG_PDL only.  Kept as the
+ * dsa_indexer_qk_prepare_store; flags may hold DSA_FLAG_PDL and
+ * DSA_FLAG_CACHE_TOKEN_MAJOR only.  Kept as the
  * baseline the fused call is measured against.
  */
 size_t dsa_unfused_workspace_bytes(int32_t T, int32_t H);

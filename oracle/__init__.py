@@ -62,11 +62,11 @@ def _load():
         lib.oracle_quantize_vector.argtypes = [P, P]
         lib.oracle_quantize_vector.restype = ctypes.c_int
         lib.oracle_k_prepare_store.argtypes = [
-            I64, P, I64, P, P, P, P, I64, I64, P, P, F32, P, I64, I32, I32, I32, I32, P]
+            I64, P, I64, P, P, P, P, I64, I64, P, P, F32, P, I64, I32, I32, I32, I32, P, I32]
         lib.oracle_k_prepare_store.restype = ctypes.c_int
         lib.oracle_qk_prepare_store.argtypes = [
             I64, I32, P, I64, I64, P, I64, P, I64, P, P, P, P, I64, I64, P, P, F32, F32,
-            P, P, P, I64, I32, I32, I32, P, P]
+            P, P, P, I64, I32, I32, I32, P, P, I32]
         lib.oracle_qk_prepare_store.restype = ctypes.c_int
         lib.oracle_qk_prepare_store_chain.argtypes = lib.oracle_qk_prepare_store.argtypes
         lib.oracle_qk_prepare_store_chain.restype = ctypes.c_int
@@ -161,9 +161,10 @@ def quantize_vector(z) -> tuple[np.ndarray, int]:
 
 def k_prepare_store(k, k_stride_t, positions, slots, cos_t, sin_t, cs_stride,
                     max_position, gamma, beta, eps, cache, num_pages, page_size,
-                    rope_dim, style, bf16_intermediate=False, T=None):
+                    rope_dim, style, bf16_intermediate=False, T=None, token_major=False):
     """k-only prepare-and-store.  ``k`` holds bf16 bit patterns (uint16) with
-    row stride ``k_stride_t`` elements; ``cache`` (uint8) is written in place.
+    row stride ``k_stride_t`` elements; ``cache`` (uint8) is written in place,
+    page-blocked or (token_major) 132 bytes per slot.
     Returns (err_bits, k_scale_exp[T])."""
     lib = _load()
     positions = _req(positions, np.int64)
@@ -177,14 +178,15 @@ def k_prepare_store(k, k_stride_t, positions, slots, cos_t, sin_t, cs_stride,
     err = lib.oracle_k_prepare_store(
         T, _ptr(k), k_stride_t, _ptr(positions), _ptr(slots), _ptr(cos_t), _ptr(sin_t),
         cs_stride, max_position, _ptr(gamma), _ptr(beta), eps, _ptr(cache), num_pages,
-        page_size, rope_dim, style, int(bool(bf16_intermediate)), _ptr(exps))
+        page_size, rope_dim, style, int(bf16_intermediate), _ptr(exps), int(bool(token_major)))
     return err, exps[:T]
 
 
 def qk_prepare_store(q, q_stride_t, q_stride_h, k, k_stride_t, w, w_stride_t,
                      positions, slots, cos_t, sin_t, cs_stride, max_position,
                      gamma, beta, eps, softmax_scale, q_fp8, weights, cache,
-                     num_pages, page_size, H, rope_dim, style, T=None, chain=False):
+                     num_pages, page_size, H, rope_dim, style, T=None, chain=False,
+                     token_major=False):
     """Fused Q/K prepare-and-store.  q/k/w are bf16 bit patterns (uint16)
     with the given strides in elements.  ``q_fp8`` ([T, H, 128] uint8),
     ``weights`` ([T, H] fp32) and ``cache`` (uint8) are written in place.
@@ -210,5 +212,6 @@ def qk_prepare_store(q, q_stride_t, q_stride_h, k, k_stride_t, w, w_stride_t,
         T, H, _ptr(q), q_stride_t, q_stride_h, _ptr(k), k_stride_t, _ptr(w), w_stride_t,
         _ptr(positions), _ptr(slots), _ptr(cos_t), _ptr(sin_t), cs_stride, max_position,
         _ptr(gamma), _ptr(beta), eps, softmax_scale, _ptr(q_fp8), _ptr(weights),
-        _ptr(cache), num_pages, page_size, rope_dim, style, _ptr(qe), _ptr(ke))
+        _ptr(cache), num_pages, page_size, rope_dim, style, _ptr(qe), _ptr(ke),
+        int(bool(token_major)))
     return err, qe[:T], ke[:T]

@@ -36,7 +36,8 @@
  *   - weights = w * 2^e_q * softmax_scale * H^-0.5, in double, rounded once
  *     (the constants of the fold: parity unpinned).
  *   - index-K cache page p holds page_size*128 code bytes, then page_size
- *     fp32 scales; slot s lives in page s / page_size at offset s % page_size.
+ *     fp32 scales; slot s lives in page s / page_size at offset s % page_size
+ *     (the other layout: 132 bytes per slot, codes then scale).
  *
  * Build: plain C99, -O2 -ffp-contract=off (no fused multiply-add except the
  * explicit fmaf calls the RoPE form asks for).
@@ -168,13 +169,22 @@ int oracle_quantize_vector(const float* z, uint8_t* codes) {
 
 /* [FUSE-QK] Motivation ("the index-K cache write") and Modifications (the
  * sliced out_cache_loc): store the codes and the fp32 scale of one k vector
- * into its slot of the paged index-K cache. */
+ * into its slot of the paged index-K cache.  Checklist ("both paged
+ * layouts"): token_major == 0 is the page-blocked layout (a page's codes,
+ * then its scales); token_major == 1 gives each slot 132 consecutive bytes,
+ * its codes then its scale. */
 static void store_index_k(uint8_t* cache, int64_t slot, int32_t page_size,
-                          const uint8_t* codes, int e) {
+                          const uint8_t* codes, int e, int token_major) {
+  float scale = (float)ldexp(1.0, e);
+  if (token_major) {
+    uint8_t* row = cache + slot * (DSA_D + 4);
+    memcpy(row, codes, DSA_D);
+    memcpy(row + DSA_D, &scale, 4);
+    return;
+  }
   int64_t page = slot / page_size, off = slot % page_size;
   uint8_t* page_base = cache + page * (int64_t)page_size * (DSA_D + 4);
   memcpy(page_base + off * DSA_D, codes, DSA_D);
-  float scale = (float)ldexp(1.0, e);
   memcpy(page_base + (int64_t)page_size * DSA_D + off * 4, &scale, 4);
 }
 
@@ -214,7 +224,8 @@ int oracle_k_prepare_store(int64_t T, const uint16_t* k, int64_t k_stride_t,
                            const float* gamma, const float* beta, float eps,
                            uint8_t* cache, int64_t num_pages, int32_t page_size,
                            int32_t rope_dim, int32_t style,
-                           int32_t bf16_intermediate, int32_t* k_scale_exp) {
+                           int32_t bf16_intermediate, int32_t* k_scale_exp,
+                           int32_t token_major) {
   int err = 0;
   for (int64_t t = 0; t < T; ++t) {
     int64_t pos = positions[t];
@@ -232,7 +243,7 @@ int oracle_k_prepare_store(int64_t T, const uint16_t* k, int64_t k_stride_t,
       err |= 2;
       continue;
     }
-    store_index_k(cache, slot, page_size, codes, e);
+    store_index_k(cache, slot, page_size, codes, e, token_major);
   }
   return err;
 }
@@ -248,7 +259,7 @@ static int qk_prepare_store(
     const float* beta, float eps, float softmax_scale, uint8_t* q_fp8,
     float* weights, uint8_t* cache, int64_t num_pages, int32_t page_size,
     int32_t rope_dim, int32_t style, int32_t* q_scale_exp,
-    int32_t* k_scale_exp, int chain) {
+    int32_t* k_scale_exp, int chain, int32_t token_major) {
   int err = 0;
   double head_factor = 1.0 / sqrt((double)H);
   for (int64_t t = 0; t < T; ++t) {
@@ -276,7 +287,8 @@ static int qk_prepare_store(
                                   positions + t, slots + t, cos_t, sin_t,
                                   cs_stride, max_position, gamma, beta, eps,
                                   cache, num_pages, page_size, rope_dim, style,
-                                  chain ? 2 : 0, k_scale_exp ? k_scale_exp + t : NULL);
+                                  chain ? 2 : 0, k_scale_exp ? k_scale_exp + t : NULL,
+                                  token_major);
   }
   return err;
 }
@@ -295,12 +307,12 @@ int oracle_qk_prepare_store(
     const float* beta, float eps, float softmax_scale, uint8_t* q_fp8,
     float* weights, uint8_t* cache, int64_t num_pages, int32_t page_size,
     int32_t rope_dim, int32_t style, int32_t* q_scale_exp,
-    int32_t* k_scale_exp) {
+    int32_t* k_scale_exp, int32_t token_major) {
   return qk_prepare_store(T, H, q, q_stride_t, q_stride_h, k, k_stride_t, w,
                           w_stride_t, positions, slots, cos_t, sin_t, cs_stride,
                           max_position, gamma, beta, eps, softmax_scale, q_fp8,
                           weights, cache, num_pages, page_size, rope_dim, style,
-                          q_scale_exp, k_scale_exp, 0);
+                          q_scale_exp, k_scale_exp, 0, token_major);
 }
 
 /* The same outputs as written by the four-launch chain of [FUSE-QK] Profile,
@@ -315,10 +327,10 @@ int oracle_qk_prepare_store_chain(
     const float* beta, float eps, float softmax_scale, uint8_t* q_fp8,
     float* weights, uint8_t* cache, int64_t num_pages, int32_t page_size,
     int32_t rope_dim, int32_t style, int32_t* q_scale_exp,
-    int32_t* k_scale_exp) {
+    int32_t* k_scale_exp, int32_t token_major) {
   return qk_prepare_store(T, H, q, q_stride_t, q_stride_h, k, k_stride_t, w,
                           w_stride_t, positions, slots, cos_t, sin_t, cs_stride,
                           max_position, gamma, beta, eps, softmax_scale, q_fp8,
                           weights, cache, num_pages, page_size, rope_dim, style,
-                          q_scale_exp, k_scale_exp, 1);
+                          q_scale_exp, k_scale_exp, 1, token_major);
 }

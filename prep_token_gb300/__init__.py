@@ -24,7 +24,7 @@ from ._build import LIB_PATH
 
 __all__ = [
     "DsaError", "NEOX", "GPTJ", "HEAD_DIM", "DEVERR_POSITION", "DEVERR_SLOT", "DEVERR_TIMEOUT",
-    "FLAG_PDL", "FLAG_PIPELINE", "FLAG_DIRECT", "FLAG_PDL_EARLY_ROPE",
+    "FLAG_PDL", "FLAG_PIPELINE", "FLAG_DIRECT", "FLAG_PDL_EARLY_ROPE", "FLAG_CACHE_TOKEN_MAJOR",
     "dsa_indexer_qk_prepare_store", "dsa_indexer_k_prepare_store", "dsa_status_string",
     "dsa_indexer_qk_prepare_store_unfused", "dsa_unfused_workspace_bytes",
     "dsa_indexer_qk_prepare_store_unfused_noalloc",
@@ -35,6 +35,8 @@ NEOX, GPTJ = 0, 1
 HEAD_DIM = 128
 DEVERR_POSITION, DEVERR_SLOT, DEVERR_TIMEOUT = 1, 2, 4
 FLAG_PDL, FLAG_PIPELINE, FLAG_DIRECT, FLAG_PDL_EARLY_ROPE = 1, 2, 4, 8
+FLAG_CACHE_TOKEN_MAJOR = 16
+_LAYOUT_FLAGS = {"paged": 0, "token_major": FLAG_CACHE_TOKEN_MAJOR}
 _KERNEL_FLAGS = {"auto": 0, "pipeline": FLAG_PIPELINE, "direct": FLAG_DIRECT}
 ROW_BYTES = HEAD_DIM + 4  # 128 codes + one fp32 scale per slot
 
@@ -133,6 +135,12 @@ def _num_pages(index_k_cache: torch.Tensor, page_size: int) -> int:
     return nbytes // (page_size * ROW_BYTES)
 
 
+def _layout(cache_layout: str) -> int:
+    if cache_layout not in _LAYOUT_FLAGS:
+        raise ValueError(f"cache_layout must be one of {sorted(_LAYOUT_FLAGS)}")
+    return _LAYOUT_FLAGS[cache_layout]
+
+
 def _flags(pdl, kernel: str) -> int:
     """pdl: False, True, or "early" (PDL plus FLAG_PDL_EARLY_ROPE: positions,
     slots and the cos/sin cache are not written by the previous kernel)."""
@@ -216,7 +224,8 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
                                  ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
                                  page_size, rope_dim=64, rope_style=NEOX, *, q_fp8_out=None,
                                  weights_out=None, err_flags=None, num_tokens=None,
-                                 max_position=None, pdl=False, kernel="auto", stream=None):
+                                 max_position=None, pdl=False, kernel="auto",
+                                 cache_layout="paged", stream=None):
     """Fused Q/K prepare-and-store (one kernel launch).
 
     q [T, H, 128] bf16, k [T, 128] bf16, w [T, H] bf16 (row strides of any
@@ -231,13 +240,15 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
     (only when the previous kernel does not write them).
     ``kernel`` = "auto" | "direct" | "pipeline" overrides the size-based
     choice between the two kernels (same bytes either way).
+    ``cache_layout`` = "paged" (a page's codes, then its scales) or
+    "token_major" (132 bytes per slot: codes, then scale).
     Returns (q_fp8 [T, H, 128] float8_e4m3fn, weights [T, H] fp32)."""
     args, outs, _, _ = _qk_args(q, k, w, positions, out_cache_loc, cos_cache, sin_cache,
                                 ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
                                 page_size, rope_dim, rope_style, q_fp8_out, weights_out,
                                 num_tokens, max_position)
     st = library().dsa_indexer_qk_prepare_store(
-        *args, _flags(pdl, kernel), _ptr(err_flags), _stream(stream))
+        *args, _flags(pdl, kernel) | _layout(cache_layout), _ptr(err_flags), _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store")
     return outs
@@ -253,7 +264,8 @@ def dsa_indexer_qk_prepare_store_unfused(q, k, w, positions, out_cache_loc, cos_
                                          index_k_cache, page_size, rope_dim=64,
                                          rope_style=NEOX, *, q_fp8_out=None, weights_out=None,
                                          workspace=None, err_flags=None, num_tokens=None,
-                                         max_position=None, pdl=False, stream=None):
+                                         max_position=None, pdl=False, cache_layout="paged",
+                                         stream=None):
     """The same computation as four launches (LayerNorm, RoPE, q quant + fold,
     k quant + store) with bf16 intermediates in ``workspace`` (a CUDA uint8
     tensor of at least dsa_unfused_workspace_bytes(T, H) bytes; allocated here
@@ -269,8 +281,8 @@ def dsa_indexer_qk_prepare_store_unfused(q, k, w, positions, out_cache_loc, cos_
         raise ValueError("workspace must be a contiguous CUDA tensor")
     nbytes = workspace.numel() * workspace.element_size()
     st = library().dsa_indexer_qk_prepare_store_unfused(
-        *args, FLAG_PDL if pdl else 0, _ptr(workspace), nbytes, _ptr(err_flags),
-        _stream(stream))
+        *args, (FLAG_PDL if pdl else 0) | _layout(cache_layout), _ptr(workspace), nbytes,
+        _ptr(err_flags), _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store_unfused")
     return outs
@@ -281,7 +293,8 @@ def dsa_indexer_qk_prepare_store_unfused_noalloc(q, k, w, positions, out_cache_l
                                                  softmax_scale, index_k_cache, page_size,
                                                  rope_dim=64, rope_style=NEOX, *, q_fp8_out,
                                                  weights_out, err_flags=None, num_tokens=None,
-                                                 max_position=None, pdl=False, stream=None):
+                                                 max_position=None, pdl=False,
+                                                 cache_layout="paged", stream=None):
     """The unfused chain with its intermediates in the library's own 32 MiB
     device buffer, for callers that cannot allocate device memory when they
     run it (an engine whose memory pool owns the whole GPU, a plugin handed
@@ -296,7 +309,8 @@ def dsa_indexer_qk_prepare_store_unfused_noalloc(q, k, w, positions, out_cache_l
                                 page_size, rope_dim, rope_style, q_fp8_out, weights_out,
                                 num_tokens, max_position)
     st = library().dsa_indexer_qk_prepare_store_unfused_noalloc(
-        *args, FLAG_PDL if pdl else 0, _ptr(err_flags), _stream(stream))
+        *args, (FLAG_PDL if pdl else 0) | _layout(cache_layout), _ptr(err_flags),
+        _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store_unfused_noalloc")
     return outs
@@ -305,7 +319,8 @@ def dsa_indexer_qk_prepare_store_unfused_noalloc(q, k, w, positions, out_cache_l
 def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
                                 ln_beta, ln_eps, index_k_cache, page_size, rope_dim=64,
                                 rope_style=NEOX, *, err_flags=None, num_tokens=None,
-                                max_position=None, pdl=False, kernel="auto", stream=None):
+                                max_position=None, pdl=False, kernel="auto",
+                                cache_layout="paged", stream=None):
     """k-only prepare-and-store (one kernel launch); writes the cache in place."""
     cs_stride, rows = _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
                                 ln_beta, index_k_cache, rope_dim)
@@ -321,6 +336,7 @@ def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cach
         _ptr(cos_cache) if rope_dim else None, _ptr(sin_cache) if rope_dim else None,
         cs_stride, max_position, _ptr(ln_gamma), _ptr(ln_beta), float(ln_eps),
         _ptr(index_k_cache), _num_pages(index_k_cache, page_size), page_size, T, HEAD_DIM,
-        rope_dim, int(rope_style), _flags(pdl, kernel), _ptr(err_flags), _stream(stream))
+        rope_dim, int(rope_style), _flags(pdl, kernel) | _layout(cache_layout), _ptr(err_flags),
+        _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_k_prepare_store")

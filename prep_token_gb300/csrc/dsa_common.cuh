@@ -429,19 +429,55 @@ __device__ __forceinline__ void quantize_slice(const float (&x)[16], int e, uint
   }
 }
 
-template <int STYLE, int RP>
+// Store the lane's codes to a 128-byte row whose start is ROW_ALIGN-aligned.
+template <int STYLE, int RP, int ROW_ALIGN = 16>
 __device__ __forceinline__ void store_slice(uint8_t* row, int l, const uint32_t* wa,
                                             const uint32_t* wb, const uint32_t* wp) {
   using S = Slice<STYLE, RP>;
+  constexpr int AA = S::ALIGN_A_U8 < ROW_ALIGN ? S::ALIGN_A_U8 : ROW_ALIGN;
+  constexpr int AB = S::ALIGN_B_U8 < ROW_ALIGN ? S::ALIGN_B_U8 : ROW_ALIGN;
+  constexpr int AP = S::ALIGN_P_U8 < ROW_ALIGN ? S::ALIGN_P_U8 : ROW_ALIGN;
   if constexpr (RP > 0) {
     if constexpr (S::NEOX) {
-      store_codes<RP, S::ALIGN_A_U8>(row + RP * l, wa);
-      store_codes<RP, S::ALIGN_B_U8>(row + S::B_BASE + RP * l, wb);
+      store_codes<RP, AA>(row + RP * l, wa);
+      store_codes<RP, AB>(row + S::B_BASE + RP * l, wb);
     } else {
-      store_codes<2 * RP, S::ALIGN_A_U8>(row + 2 * RP * l, wa);
+      store_codes<2 * RP, AA>(row + 2 * RP * l, wa);
     }
   }
-  if constexpr (S::NP > 0) store_codes<S::NP, S::ALIGN_P_U8>(row + S::P_BASE + S::NP * l, wp);
+  if constexpr (S::NP > 0) store_codes<S::NP, AP>(row + S::P_BASE + S::NP * l, wp);
+}
+
+// Index-K cache geometry and the store of one key's codes and scale into it.
+//   page-blocked (default): page p holds page_size rows of 128 codes, then
+//     page_size fp32 scales; slot s = row s % page_size of page s / page_size;
+//   token-major (DSA_FLAG_CACHE_TOKEN_MAJOR): slot s owns bytes
+//     [132 s, 132 s + 132): 128 codes, then its fp32 scale.
+struct CacheGeom {
+  uint8_t* cache;
+  long long num_slots;
+  long long page_bytes;  // page_size * 132
+  int page_size;
+  int token_major;
+};
+
+template <int STYLE, int RP>
+__device__ __forceinline__ void store_index_k(const CacheGeom& g, long long slot, int l,
+                                              const uint32_t* wa, const uint32_t* wb,
+                                              const uint32_t* wp, int e) {
+  if (g.token_major) {
+    uint8_t* row = g.cache + slot * (kD + 4);
+    store_slice<STYLE, RP, 4>(row, l, wa, wb, wp);
+    if (l == 0) *reinterpret_cast<float*>(row + kD) = pow2f(e);
+  } else {
+    const long long page = slot / g.page_size;
+    const long long off = slot - page * g.page_size;
+    uint8_t* base = g.cache + page * g.page_bytes;
+    store_slice<STYLE, RP>(base + off * kD, l, wa, wb, wp);
+    if (l == 0)
+      *reinterpret_cast<float*>(base + static_cast<long long>(g.page_size) * kD + 4 * off) =
+          pow2f(e);
+  }
 }
 
 // y = x * rstd * gamma + beta on n values whose gamma/beta start at `row`

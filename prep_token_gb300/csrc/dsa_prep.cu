@@ -66,10 +66,7 @@ struct Params {
   float fold;  // softmax_scale * H^-0.5, rounded once to fp32
   uint8_t* q_out;
   float* w_out;
-  uint8_t* cache;
-  long long num_slots;
-  long long page_bytes;  // page_size * 132
-  int page_size;
+  CacheGeom cg;
   int T;
   int H;
   int rope_dim;
@@ -132,16 +129,11 @@ __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const R
     if (l == 0) raise_error(p, DSA_DEVERR_POSITION);
     return;
   }
-  if (slot < 0 || slot >= p.num_slots) {
+  if (slot < 0 || slot >= p.cg.num_slots) {
     if (l == 0) raise_error(p, DSA_DEVERR_SLOT);
     return;
   }
-  const long long page = slot / p.page_size;
-  const long long off = slot - page * p.page_size;
-  uint8_t* base = p.cache + page * p.page_bytes;
-  store_slice<STYLE, RP>(base + off * kD, l, wa, wb, wp);
-  if (l == 0)
-    *reinterpret_cast<float*>(base + static_cast<long long>(p.page_size) * kD + 4 * off) = pow2f(e);
+  store_index_k<STYLE, RP>(p.cg, slot, l, wa, wb, wp, e);
 }
 
 // ================================================================ direct kernel
@@ -536,6 +528,7 @@ cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligne
     cfg.numAttrs = 1;
   }
   p.early_rope = (flags & DSA_FLAG_PDL_EARLY_ROPE) ? 1 : 0;
+  p.cg.token_major = (flags & DSA_FLAG_CACHE_TOKEN_MAJOR) ? 1 : 0;
   const long long vecs = static_cast<long long>(p.T) * (p.H > 0 ? p.H : 1);
   bool direct = vecs <= kDirectMaxVectors;
   if (flags & DSA_FLAG_PIPELINE) direct = false;
@@ -572,7 +565,7 @@ dsa_status check_k_side(const void* k, int64_t k_stride_t, const int64_t* positi
   if (rp_index(rope_dim) < 0) return DSA_ERR_UNSUPPORTED;
   if (rope_style != DSA_ROPE_NEOX && rope_style != DSA_ROPE_GPTJ) return DSA_ERR_UNSUPPORTED;
   if (flags & ~static_cast<uint32_t>(DSA_FLAG_PDL | DSA_FLAG_PIPELINE | DSA_FLAG_DIRECT |
-                                     DSA_FLAG_PDL_EARLY_ROPE))
+                                     DSA_FLAG_PDL_EARLY_ROPE | DSA_FLAG_CACHE_TOKEN_MAJOR))
     return DSA_ERR_UNSUPPORTED;
   if ((flags & DSA_FLAG_PDL_EARLY_ROPE) && !(flags & DSA_FLAG_PDL)) return DSA_ERR_UNSUPPORTED;
   if ((flags & DSA_FLAG_PIPELINE) && (flags & DSA_FLAG_DIRECT)) return DSA_ERR_UNSUPPORTED;
@@ -586,7 +579,7 @@ dsa_status check_k_side(const void* k, int64_t k_stride_t, const int64_t* positi
     return DSA_ERR_NULL;
   if (rope_dim > 0 && (!cos_cache || !sin_cache)) return DSA_ERR_NULL;
   if (rope_dim > 0 && cs_stride < rope_dim / 2) return DSA_ERR_SHAPE;
-  if (page_size % 4 != 0) return DSA_ERR_ALIGN;
+  if (page_size % 4 != 0 && !(flags & DSA_FLAG_CACHE_TOKEN_MAJOR)) return DSA_ERR_ALIGN;
   if (misaligned(k, 16) || k_stride_t % 8 != 0) return DSA_ERR_ALIGN;
   if (misaligned(positions, 8) || misaligned(out_cache_loc, 8)) return DSA_ERR_ALIGN;
   if (misaligned(ln_gamma, 16) || misaligned(ln_beta, 16)) return DSA_ERR_ALIGN;
@@ -613,10 +606,10 @@ void fill_k_side(Params& p, const void* k, int64_t k_stride_t, const int64_t* po
   p.gamma = ln_gamma;
   p.beta = ln_beta;
   p.eps = ln_eps;
-  p.cache = static_cast<uint8_t*>(index_k_cache);
-  p.num_slots = num_pages * page_size;
-  p.page_size = page_size;
-  p.page_bytes = static_cast<long long>(page_size) * (kD + 4);
+  p.cg.cache = static_cast<uint8_t*>(index_k_cache);
+  p.cg.num_slots = num_pages * page_size;
+  p.cg.page_size = page_size;
+  p.cg.page_bytes = static_cast<long long>(page_size) * (kD + 4);
   p.T = T;
   p.rope_dim = rope_dim;
   p.cs_bytes = rope_dim * 2;

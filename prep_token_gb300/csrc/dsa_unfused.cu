@@ -45,10 +45,7 @@ struct UParams {
   float fold;  // softmax_scale * H^-0.5, rounded once to fp32
   uint8_t* q_out;
   float* w_out;
-  uint8_t* cache;
-  long long num_slots;
-  long long page_bytes;
-  int page_size;
+  CacheGeom cg;
   int T;
   int H;
   int rope_dim;
@@ -226,16 +223,11 @@ __global__ void __launch_bounds__(kThreads) unfused_k_quant_store_kernel(const U
     if (l == 0 && p.err) atomicOr(p.err, DSA_DEVERR_POSITION);
     return;
   }
-  if (slot < 0 || slot >= p.num_slots) {
+  if (slot < 0 || slot >= p.cg.num_slots) {
     if (l == 0 && p.err) atomicOr(p.err, DSA_DEVERR_SLOT);
     return;
   }
-  const long long page = slot / p.page_size;
-  const long long off = slot - page * p.page_size;
-  uint8_t* base = p.cache + page * p.page_bytes;
-  store_slice<0, 0>(base + off * kD, l, wa, wb, wp);
-  if (l == 0)
-    *reinterpret_cast<float*>(base + static_cast<long long>(p.page_size) * kD + 4 * off) = pow2f(e);
+  store_index_k<0, 0>(p.cg, slot, l, wa, wb, wp, e);
 }
 
 // ---------------------------------------------------------------- host side
@@ -302,7 +294,8 @@ dsa_status dsa_indexer_qk_prepare_store_unfused(
   if (T < 0 || H < 1 || H > 4096) return DSA_ERR_SHAPE;
   if (head_dim != kD || rope_index(rope_dim) < 0) return DSA_ERR_UNSUPPORTED;
   if (rope_style != DSA_ROPE_NEOX && rope_style != DSA_ROPE_GPTJ) return DSA_ERR_UNSUPPORTED;
-  if (flags & ~static_cast<uint32_t>(DSA_FLAG_PDL)) return DSA_ERR_UNSUPPORTED;
+  if (flags & ~static_cast<uint32_t>(DSA_FLAG_PDL | DSA_FLAG_CACHE_TOKEN_MAJOR))
+    return DSA_ERR_UNSUPPORTED;
   if (!(ln_eps >= 0.0f) || !std::isfinite(ln_eps) || !std::isfinite(softmax_scale))
     return DSA_ERR_UNSUPPORTED;
   if (page_size < 1 || num_pages < 1 || max_position < 1) return DSA_ERR_SHAPE;
@@ -316,7 +309,7 @@ dsa_status dsa_indexer_qk_prepare_store_unfused(
   if (rope_dim > 0 && (!cos_cache || !sin_cache)) return DSA_ERR_NULL;
   if (rope_dim > 0 && cs_stride < rope_dim / 2) return DSA_ERR_SHAPE;
   if (workspace_bytes < dsa_unfused_workspace_bytes(T, H)) return DSA_ERR_SHAPE;
-  if (page_size % 4 != 0) return DSA_ERR_ALIGN;
+  if (page_size % 4 != 0 && !(flags & DSA_FLAG_CACHE_TOKEN_MAJOR)) return DSA_ERR_ALIGN;
   if (misaligned(q, 16) || q_stride_t % 8 != 0 || q_stride_h % 8 != 0) return DSA_ERR_ALIGN;
   if (misaligned(k, 16) || k_stride_t % 8 != 0 || misaligned(w, 2)) return DSA_ERR_ALIGN;
   if (misaligned(positions, 8) || misaligned(out_cache_loc, 8)) return DSA_ERR_ALIGN;
@@ -348,10 +341,11 @@ dsa_status dsa_indexer_qk_prepare_store_unfused(
   p.fold = static_cast<float>(static_cast<double>(softmax_scale) / std::sqrt(static_cast<double>(H)));
   p.q_out = static_cast<uint8_t*>(q_fp8_out);
   p.w_out = weights_out;
-  p.cache = static_cast<uint8_t*>(index_k_cache);
-  p.num_slots = num_pages * page_size;
-  p.page_bytes = static_cast<long long>(page_size) * (kD + 4);
-  p.page_size = page_size;
+  p.cg.cache = static_cast<uint8_t*>(index_k_cache);
+  p.cg.num_slots = num_pages * page_size;
+  p.cg.page_bytes = static_cast<long long>(page_size) * (kD + 4);
+  p.cg.page_size = page_size;
+  p.cg.token_major = (flags & DSA_FLAG_CACHE_TOKEN_MAJOR) ? 1 : 0;
   p.T = T;
   p.H = H;
   p.rope_dim = rope_dim;

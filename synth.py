@@ -62,6 +62,7 @@ class Inputs:
     eps: float = 1e-6
     softmax_scale: float = float(np.float32(D ** -0.5))
     kw: np.ndarray | None = None
+    token_major: bool = False   # index-K cache layout: 132 bytes per slot
 
     @property
     def q_stride_t(self):

@@ -34,7 +34,13 @@ def new_cache(inp, device="cuda", fill=SENTINEL):
     return torch.full((inp.cache_bytes,), fill, dtype=torch.uint8, device=device)
 
 
+def _layout_kw(inp, kw):
+    kw.setdefault("cache_layout", "token_major" if inp.token_major else "paged")
+    return kw
+
+
 def run_qk(inp, d, cache=None, err=None, **kw):
+    kw = _layout_kw(inp, kw)
     cache = new_cache(inp) if cache is None else cache
     q_fp8, weights = dp.dsa_indexer_qk_prepare_store(
         d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
@@ -46,6 +52,7 @@ def run_qk(inp, d, cache=None, err=None, **kw):
 
 
 def run_k(inp, d, cache=None, err=None, **kw):
+    kw = _layout_kw(inp, kw)
     cache = new_cache(inp) if cache is None else cache
     dp.dsa_indexer_k_prepare_store(
         d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"], inp.eps,

@@ -36,7 +36,7 @@ def run_oracle_qk(inp, cache=None, T=None, chain=False):
         inp.positions[:T], inp.slots[:T], inp.cos, inp.sin, inp.cs_stride,
         inp.max_position, inp.gamma, inp.beta, inp.eps, inp.softmax_scale,
         q_fp8, weights, cache, inp.num_pages, inp.page_size, inp.H, inp.rope_dim,
-        inp.style, T=T, chain=chain)
+        inp.style, T=T, chain=chain, token_major=inp.token_major)
     return dict(q_fp8=q_fp8[:T], weights=weights[:T], cache=cache, err=err,
                 q_exp=qe, k_exp=ke)
 
@@ -48,13 +48,17 @@ def run_oracle_k(inp, cache=None, bf16_intermediate=False, T=None):
         inp.k_buffer().reshape(-1), inp.k_stride_t, inp.positions[:T], inp.slots[:T],
         inp.cos, inp.sin, inp.cs_stride, inp.max_position, inp.gamma, inp.beta,
         inp.eps, cache, inp.num_pages, inp.page_size, inp.rope_dim, inp.style,
-        bf16_intermediate=bf16_intermediate, T=T)
+        bf16_intermediate=bf16_intermediate, T=T, token_major=inp.token_major)
     return dict(cache=cache, err=err, k_exp=ke)
 
 
 def cache_views(inp, cache):
     """(codes[num_pages*page_size, 128], scales[num_pages*page_size]) of the
-    paged index-K cache: page p = [page_size x 128 codes][page_size x fp32]."""
+    index-K cache: page-blocked (page p = [page_size x 128 codes][page_size x
+    fp32]) or token-major (132 bytes per slot)."""
+    if inp.token_major:
+        rows = cache.reshape(-1, 132)
+        return rows[:, :128], np.ascontiguousarray(rows[:, 128:]).view(np.float32).reshape(-1)
     P = inp.page_size
     pages = cache.reshape(inp.num_pages, P * 132)
     codes = pages[:, :P * 128].reshape(inp.num_pages * P, 128)

@@ -68,7 +68,7 @@ def _k(lib, **over):
     (dict(k=None), 1), (dict(pos=None), 1), (dict(cache=None), 1), (dict(cos=None), 1),
     (dict(ps=6), 2), (dict(k=A + 8), 2), (dict(skt=132), 2), (dict(pos=A + 4), 2),
     (dict(g=A + 4), 2), (dict(cache=A + 8), 2), (dict(cos=A + 4), 2), (dict(cs=34), 2),
-    (dict(cs=16), 3), (dict(skt=-128), 3), (dict(flags=16), 4), (dict(flags=6), 4), (dict(flags=8), 4), (dict(flags=0x80000000), 4),
+    (dict(cs=16), 3), (dict(skt=-128), 3), (dict(flags=32), 4), (dict(flags=6), 4), (dict(flags=8), 4), (dict(flags=0x80000000), 4),
     (dict(r=48), 4), (dict(r=96), 4), (dict(r=112), 4),
 ])
 def test_k_side_validation(lib, over, status):
@@ -120,7 +120,7 @@ def test_unfused_workspace_size(lib):
 
 @pytest.mark.parametrize("over,status", [
     (dict(T=-1), 3), (dict(H=0), 3), (dict(D=64), 4), (dict(r=48), 4), (dict(style=3), 4),
-    (dict(flags=2), 4), (dict(ws=None), 1), (dict(wsb=1000), 3), (dict(ws=0x100000 + 16), 2),
+    (dict(flags=2), 4), (dict(flags=32), 4), (dict(ws=None), 1), (dict(wsb=1000), 3), (dict(ws=0x100000 + 16), 2),
     (dict(q=A + 2), 2), (dict(cache=None), 1), (dict(ps=6), 2), (dict(swt=8), 3),
 ])
 def test_unfused_validation(lib, over, status):

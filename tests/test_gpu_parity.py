@@ -294,3 +294,20 @@ def test_head_stride_not_contiguous_uses_per_head_copies():
     for key in ("q_fp8", "weights", "cache"):
         assert np.array_equal(got[key], ref[key]), key
     assert_parity(b, got, run_oracle_qk(b))
+
+
+@pytest.mark.parametrize("page_size", [1, 3, 64])
+@pytest.mark.parametrize("style", [synth.NEOX, synth.GPTJ])
+def test_token_major_cache_layout(page_size, style):
+    """The second index-K layout (132 bytes per slot), through both kernels
+    and the k-only path; page sizes that are not multiples of 4 are allowed."""
+    inp = synth.make_decode(seed=50 + page_size, T=70, H=16, style=style)
+    inp.page_size, inp.num_pages = page_size, (4096 * 64) // page_size
+    inp.token_major = True
+    _check(inp)
+
+
+def test_token_major_prefill_full_size():
+    inp = synth.make_prefill()
+    inp.token_major = True
+    _check(inp, kernels=("pipeline",))

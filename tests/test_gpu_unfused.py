@@ -24,6 +24,7 @@ def _cuda():
 
 def run_unfused(inp, d, cache=None, err=None, **kw):
     import prep_token_gb300 as dp
+    kw.setdefault("cache_layout", "token_major" if inp.token_major else "paged")
     cache = new_cache(inp) if cache is None else cache
     q_fp8, weights = dp.dsa_indexer_qk_prepare_store_unfused(
         d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
@@ -123,3 +124,11 @@ def test_pdl_graph_matches_eager():
     assert np.array_equal(q_out.view(torch.uint8).cpu().numpy(), eager["q_fp8"])
     assert np.array_equal(w_out.cpu().numpy(), eager["weights"])
     assert np.array_equal(cache.cpu().numpy(), eager["cache"])
+
+
+@pytest.mark.parametrize("page_size", [1, 64])
+def test_token_major_cache_layout(page_size):
+    inp = synth.make_decode(seed=60 + page_size, T=50, H=8)
+    inp.page_size, inp.num_pages = page_size, (4096 * 64) // page_size
+    inp.token_major = True
+    _check(inp)

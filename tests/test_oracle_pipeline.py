@@ -272,3 +272,42 @@ def test_chain_mode_differs_from_fused_only_near_ties():
     assert same.mean() > 0.99
     d = code_distance(fused["q_fp8"][same], chain["q_fp8"][same])
     assert 0 < (d > 0).mean() < 0.06 and d.max() <= 1
+
+
+def test_worked_token_major_slot(worked):
+    ex, kx = worked["token_major_slot"], worked["k_identity"]
+    k = synth.to_bf16_bits(np.array(_expand(kx["k"]), np.float32))
+    P, NP = ex["page_size"], ex["num_pages"]
+    cache = np.full(NP * P * 132, SENTINEL, np.uint8)
+    err, ke = oracle.k_prepare_store(
+        k, 128, np.array([0], np.int64), np.array([ex["slot"]], np.int64),
+        np.ones((1, 32), np.float32), np.zeros((1, 32), np.float32), 32, 1,
+        np.ones(128, np.float32), np.zeros(128, np.float32), kx["eps"], cache, NP, P, 64,
+        oracle.NEOX, token_major=True)
+    assert err == 0 and ke[0] == kx["expect_exp"]
+    lo, hi = ex["expect_code_bytes"]
+    sb, sbytes = ex["expect_scale_bytes"]
+    assert list(cache[lo:hi]) == _expand(kx["expect_codes"])
+    assert list(cache[sb:sb + 4]) == sbytes
+    mask = np.ones(cache.size, bool)
+    mask[lo:sb + 4] = False
+    assert np.all(cache[mask] == SENTINEL)
+
+
+@pytest.mark.parametrize("page_size", [1, 3, 64])
+def test_layouts_hold_the_same_slots(page_size):
+    """The two index-K layouts differ only in where a slot's bytes sit."""
+    inp = synth.make_decode(seed=23, T=40, H=2)
+    inp.page_size, inp.num_pages = page_size, (4096 * 64) // page_size
+    if page_size % 4 == 0:
+        paged = run_oracle_qk(inp)
+        pc, ps = cache_views(inp, paged["cache"])
+    inp.token_major = True
+    tm = run_oracle_qk(inp)
+    tc, ts = cache_views(inp, tm["cache"])
+    assert np.all(tc[np.setdiff1d(np.arange(tc.shape[0]), inp.slots)] == SENTINEL)
+    if page_size % 4 == 0:
+        assert np.array_equal(tc[inp.slots], pc[inp.slots])
+        assert np.array_equal(ts[inp.slots], ps[inp.slots])
+        assert np.array_equal(tm["q_fp8"], paged["q_fp8"])
+    assert np.all((ts[inp.slots].view(np.uint32) & 0x7FFFFF) == 0)
