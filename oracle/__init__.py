@@ -70,6 +70,8 @@ def _load():
         lib.oracle_qk_prepare_store.restype = ctypes.c_int
         lib.oracle_qk_prepare_store_chain.argtypes = lib.oracle_qk_prepare_store.argtypes
         lib.oracle_qk_prepare_store_chain.restype = ctypes.c_int
+        lib.oracle_mqa_logits.argtypes = [I32, I32, P, P, P, I64, I32, P, I64, P, P, I64, I32]
+        lib.oracle_mqa_logits.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -215,3 +217,24 @@ def qk_prepare_store(q, q_stride_t, q_stride_h, k, k_stride_t, w, w_stride_t,
         _ptr(cache), num_pages, page_size, rope_dim, style, _ptr(qe), _ptr(ke),
         int(bool(token_major)))
     return err, qe[:T], ke[:T]
+
+
+def mqa_logits(q_fp8, weights, cache, num_pages, page_size, block_table, context_lens,
+               max_context):
+    """fp8 paged MQA logits (the indexer's score for each (token, key)):
+    logits[t, j] = k_scale[j] * sum_h weights[t, h] * max(q[t, h] . k[j], 0)
+    for j < context_lens[t], -inf after.  q_fp8 [T, H, 128] uint8 codes,
+    weights [T, H] fp32, cache page-blocked uint8, block_table [T, n] int32.
+    Returns (err_bits, logits [T, max_context] fp32)."""
+    lib = _load()
+    q_fp8 = _req(q_fp8, np.uint8)
+    T, H = q_fp8.shape[0], q_fp8.shape[1]
+    weights = _req(weights, np.float32)
+    cache = _req(cache, np.uint8)
+    block_table = _req(block_table, np.int32)
+    context_lens = _req(context_lens, np.int32)
+    out = np.empty((max(T, 1), max(max_context, 1)), np.float32)
+    err = lib.oracle_mqa_logits(T, H, _ptr(q_fp8), _ptr(weights), _ptr(cache), num_pages,
+                                page_size, _ptr(block_table), block_table.shape[1],
+                                _ptr(context_lens), _ptr(out), out.shape[1], max_context)
+    return err, out[:T, :max_context]

@@ -334,3 +334,56 @@ int oracle_qk_prepare_store_chain(
                           weights, cache, num_pages, page_size, rope_dim, style,
                           q_scale_exp, k_scale_exp, 1, token_major);
 }
+
+/* ------------------------------------------------------------ the consumer */
+
+/* The indexer's fp8 paged MQA logits, the kernel that reads this path's
+ * outputs ([FUSE-Q] Kernel-level evidence lists it after the index-K store as
+ * "_gluon_deepgemm_fp8_paged_mqa_logits"; the pages give no formula).  It is
+ * read from the DeepSeek sparse-attention indexer: a score per (query token,
+ * key) is the gate-weighted sum over heads of the ReLU'd dot product,
+ *   logits[t, j] = k_scale[j] * sum_h weights[t, h] * max(q[t, h] . k[j], 0)
+ * with q and k the decoded e4m3 codes; weights already hold the q scales, and
+ * since every scale is a positive power of two it moves through the ReLU.
+ * Key j of token t sits in page block_table[t][j / page_size], row
+ * j % page_size of the page-blocked index-K cache.  Columns j >= context_lens[t]
+ * (up to max_context) are -inf.  Computed in double, rounded once.  Returns 2
+ * if a block-table entry is out of range (that key's logit is then NaN). */
+int oracle_mqa_logits(int32_t T, int32_t H, const uint8_t* q_fp8,
+                      const float* weights, const uint8_t* cache,
+                      int64_t num_pages, int32_t page_size,
+                      const int32_t* block_table, int64_t bt_stride,
+                      const int32_t* context_lens, float* logits,
+                      int64_t logits_stride, int32_t max_context) {
+  int err = 0;
+  double dec[256];
+  for (int c = 0; c < 256; ++c) dec[c] = (double)oracle_e4m3_decode((uint8_t)c);
+  for (int32_t t = 0; t < T; ++t) {
+    for (int32_t j = 0; j < max_context; ++j) {
+      float* out = logits + (int64_t)t * logits_stride + j;
+      if (j >= context_lens[t]) {
+        *out = -INFINITY;
+        continue;
+      }
+      int64_t page = block_table[(int64_t)t * bt_stride + j / page_size];
+      if (page < 0 || page >= num_pages) {
+        err |= 2;
+        *out = NAN;
+        continue;
+      }
+      const uint8_t* base = cache + page * (int64_t)page_size * (DSA_D + 4);
+      const uint8_t* kc = base + (int64_t)(j % page_size) * DSA_D;
+      float kscale;
+      memcpy(&kscale, base + (int64_t)page_size * DSA_D + 4 * (j % page_size), 4);
+      double acc = 0.0;
+      for (int32_t h = 0; h < H; ++h) {
+        const uint8_t* qc = q_fp8 + ((int64_t)t * H + h) * DSA_D;
+        double dot = 0.0;
+        for (int d = 0; d < DSA_D; ++d) dot += dec[qc[d]] * dec[kc[d]];
+        acc += (double)weights[(int64_t)t * H + h] * (dot > 0.0 ? dot : 0.0);
+      }
+      *out = (float)(acc * (double)kscale);
+    }
+  }
+  return err;
+}

@@ -325,3 +325,57 @@ def algorithmic_bytes(T: int, H: int, with_q: bool = True) -> int:
     if with_q:
         return T * (3 * H * D + 6 * H + 660) + 1024
     return T * 660 + 1024
+
+
+@dataclasses.dataclass
+class LogitsInputs:
+    """Inputs of the indexer's fp8 paged MQA logits (the consumer of this
+    path's outputs): q codes [T, H, 128] (uint8 e4m3), gate weights [T, H]
+    fp32, a page-blocked index-K cache, per-token block tables and context
+    lengths."""
+    T: int
+    H: int
+    page_size: int
+    num_pages: int
+    q_fp8: np.ndarray
+    weights: np.ndarray
+    cache: np.ndarray
+    block_table: np.ndarray
+    context_lens: np.ndarray
+    max_context: int
+
+
+def random_e4m3_codes(rng, shape, max_exp_field=11):
+    """Uniform random finite e4m3 codes with exponent field <= max_exp_field
+    (so |value| <= 2^(max_exp_field - 6)), either sign; no NaN codes."""
+    mag = rng.integers(0, (max_exp_field + 1) * 8, size=shape, dtype=np.int64)
+    sign = rng.integers(0, 2, size=shape, dtype=np.int64) << 7
+    return (mag | sign).astype(np.uint8)
+
+
+def make_logits(seed=5, T=64, H=64, context=16384, page_size=64, ragged=False, spare_pages=0):
+    """Decode-step logits workload: T sequences (one query token each, H
+    indexer heads) with `context` cached keys each (or, ragged, uniform in
+    [1, context]), every sequence on its own shuffled pages; scales are
+    powers of two 2^e, e uniform in [-10, 0]."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(1, context + 1, T) if ragged else np.full(T, context)
+    blocks = (lens + page_size - 1) // page_size
+    num_pages = int(blocks.sum()) + spare_pages
+    perm = rng.permutation(num_pages).astype(np.int32)
+    max_blocks = int(blocks.max())
+    table = np.zeros((T, max_blocks), np.int32)
+    at = 0
+    for t in range(T):
+        table[t, :blocks[t]] = perm[at:at + blocks[t]]
+        at += blocks[t]
+    cache = np.empty((num_pages, page_size * (D + 4)), np.uint8)
+    cache[:, :page_size * D] = random_e4m3_codes(rng, (num_pages, page_size * D))
+    exps = rng.integers(-10, 1, (num_pages, page_size)).astype(np.uint32)
+    cache[:, page_size * D:] = ((exps + np.uint32(127)) << np.uint32(23)).view(np.uint8).reshape(
+        num_pages, page_size * 4)
+    q = random_e4m3_codes(rng, (T, H, D))
+    w = (rng.standard_normal((T, H)) * 0.05).astype(np.float32)
+    return LogitsInputs(T=T, H=H, page_size=page_size, num_pages=num_pages, q_fp8=q, weights=w,
+                        cache=cache.reshape(-1), block_table=table,
+                        context_lens=lens.astype(np.int32), max_context=int(lens.max()))
