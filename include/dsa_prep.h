@@ -251,6 +251,35 @@ dsa_status dsa_indexer_qk_prepare_store_unfused_noalloc(
     int32_t T, int32_t H, int32_t head_dim, int32_t rope_dim,
     int32_t rope_style, uint32_t flags, int32_t* err_flags, void* stream);
 
+/*
+ * fp8 paged MQA logits: the indexer kernel that reads what the calls above
+ * write.  The vllm PR "[ROCm][Perf] Enable fused indexer-Q RoPE+quant kernel
+ * for DeepSeek/GLM sparse attention" lists it (Kernel-level evidence,
+ * "_gluon_deepgemm_fp8_paged_mqa_logits") right after the index-K store and
+ * gives no formula; the one here is the DeepSeek sparse-attention indexer's:
+ *   logits[t, j] = k_scale[j] * sum_h weights[t, h] * max(q[t, h] . k[j], 0)
+ * for j < context_lens[t], with q and k the e4m3 codes (weights already hold
+ * the q scales); columns context_lens[t] <= j < max_context get -inf.
+ *
+ *   q_fp8          e4m3 [T, H, 128] contiguous, 16-byte aligned.
+ *   weights        fp32 [T, H] contiguous.
+ *   index_k_cache  page-blocked layout, page_size == 64, 16-byte aligned.
+ *   block_table    int32 [T, >= ceil(context_lens[t] / 64)], row stride
+ *                  bt_stride: the physical page of each 64-key block.
+ *   context_lens   int32 [T], keys of token t.
+ *   logits         fp32 [T, logits_stride >= max_context].
+ *   T <= 65535; H in {16, 32, 64, 128}; flags may hold DSA_FLAG_PDL.
+ * Runs on the tensor cores (tcgen05, fp32 accumulation in TMEM); the first
+ * call on a device raises its shared-memory limit there.  A block-table entry
+ * outside [0, num_pages) sets DSA_DEVERR_SLOT (its keys then read page 0).
+ */
+dsa_status dsa_indexer_mqa_logits(
+    const void* q_fp8, const float* weights,
+    const void* index_k_cache, int64_t num_pages, int32_t page_size,
+    const int32_t* block_table, int64_t bt_stride, const int32_t* context_lens,
+    float* logits, int64_t logits_stride, int32_t max_context,
+    int32_t T, int32_t H, uint32_t flags, int32_t* err_flags, void* stream);
+
 /* A static, NUL-terminated description of a status code. */
 const char* dsa_status_string(dsa_status status);
 

@@ -27,7 +27,7 @@ __all__ = [
     "FLAG_PDL", "FLAG_PIPELINE", "FLAG_DIRECT", "FLAG_PDL_EARLY_ROPE", "FLAG_CACHE_TOKEN_MAJOR",
     "dsa_indexer_qk_prepare_store", "dsa_indexer_k_prepare_store", "dsa_status_string",
     "dsa_indexer_qk_prepare_store_unfused", "dsa_unfused_workspace_bytes",
-    "dsa_indexer_qk_prepare_store_unfused_noalloc",
+    "dsa_indexer_qk_prepare_store_unfused_noalloc", "dsa_indexer_mqa_logits",
     "library", "cache_bytes", "cache_views",
 ]
 
@@ -82,6 +82,9 @@ def library() -> ctypes.CDLL:
             P, I64, I64, P, I64, P, I64, P, P, P, P, I64, I64, P, P, F32, F32, P, P, P, I64, I32,
             I32, I32, I32, I32, I32, U32, P, P]
         lib.dsa_indexer_qk_prepare_store_unfused_noalloc.restype = ctypes.c_int
+        lib.dsa_indexer_mqa_logits.argtypes = [
+            P, P, P, I64, I32, P, I64, P, P, I64, I32, I32, I32, U32, P, P]
+        lib.dsa_indexer_mqa_logits.restype = ctypes.c_int
         lib.dsa_status_string.argtypes = [ctypes.c_int]
         lib.dsa_status_string.restype = ctypes.c_char_p
         lib.dsa_prep_version.argtypes = []
@@ -340,3 +343,36 @@ def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cach
         _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_k_prepare_store")
+
+
+def dsa_indexer_mqa_logits(q_fp8, weights, index_k_cache, page_size, block_table, context_lens,
+                           max_context, *, logits=None, err_flags=None, pdl=False, stream=None):
+    """fp8 paged MQA logits on the tensor cores:
+    logits[t, j] = k_scale[j] * sum_h weights[t, h] * relu(q[t, h] . k[j])
+    for j < context_lens[t], -inf up to max_context.  q_fp8 [T, H, 128]
+    (float8_e4m3fn or uint8), weights [T, H] fp32, index_k_cache page-blocked
+    (page_size 64), block_table [T, n] int32, context_lens [T] int32.
+    Returns logits [T, max_context] fp32."""
+    if q_fp8.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise TypeError("q_fp8 must be float8_e4m3fn or uint8 codes")
+    if not q_fp8.is_cuda or not q_fp8.is_contiguous() or q_fp8.dim() != 3 \
+            or q_fp8.shape[2] != HEAD_DIM:
+        raise ValueError("q_fp8 must be a contiguous CUDA [T, H, 128] tensor")
+    T, H = q_fp8.shape[0], q_fp8.shape[1]
+    _need(weights, "weights", torch.float32, 2)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    if not weights.is_contiguous() or tuple(weights.shape) != (T, H):
+        raise ValueError("weights must be contiguous [T, H]")
+    if logits is None:
+        logits = torch.empty((T, max(int(max_context), 1)), dtype=torch.float32,
+                             device=q_fp8.device)
+    _need(logits, "logits", torch.float32, 2)
+    st = library().dsa_indexer_mqa_logits(
+        _ptr(q_fp8), _ptr(weights), _ptr(index_k_cache), _num_pages(index_k_cache, page_size),
+        page_size, _ptr(block_table), block_table.stride(0), _ptr(context_lens), _ptr(logits),
+        logits.stride(0), int(max_context), T, H, FLAG_PDL if pdl else 0, _ptr(err_flags),
+        _stream(stream))
+    if st != 0:
+        raise DsaError(st, "dsa_indexer_mqa_logits")
+    return logits[:, :max_context]

@@ -1,0 +1,109 @@
+"""fp8 paged MQA logits on the tensor cores, through the C ABI, against the
+oracle.  Tolerance, from the arithmetic: the kernel accumulates the 128-term
+dot products on the tensor cores in fp32 and the H-term weighted ReLU sum in
+fp32, so |gpu - ref| <= 2^-14 * k_scale * sum_h |w_h| * sum_d |q_hd k_d| (a
+generous multiple of the (128 + H) * 2^-24 rounding bound, which also covers
+an accumulator narrower than full fp32); masked columns must be exactly -inf."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import prep_token_gb300 as dp
+    dp.library()
+
+
+def _decode(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def _tolerance(li, tokens):
+    """2^-14 * k_scale * sum_h |w_h| * sum_d |q_hd k_d| per (token, key)."""
+    cache = li.cache.reshape(li.num_pages, -1)
+    P = li.page_size
+    tol = np.zeros((len(tokens), li.max_context))
+    for r, t in enumerate(tokens):
+        n = li.context_lens[t]
+        pages = cache[li.block_table[t, :(n + P - 1) // P]]
+        kc = pages[:, :P * 128].reshape(-1, 128)[:n]
+        ks = np.ascontiguousarray(pages[:, P * 128:]).view(np.float32).reshape(-1)[:n]
+        mass = np.abs(_decode(li.q_fp8[t])) @ np.abs(_decode(kc)).T       # [H, n]
+        tol[r, :n] = 2.0 ** -14 * ks * (np.abs(li.weights[t].astype(np.float64)) @ mass)
+    return tol
+
+
+def _run_gpu(li, err=None):
+    import prep_token_gb300 as dp
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = dp.dsa_indexer_mqa_logits(d(li.q_fp8), d(li.weights), d(li.cache), li.page_size,
+                                    d(li.block_table), d(li.context_lens), li.max_context,
+                                    err_flags=err)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def _oracle(li, tokens):
+    sub = synth.LogitsInputs(
+        T=len(tokens), H=li.H, page_size=li.page_size, num_pages=li.num_pages,
+        q_fp8=np.ascontiguousarray(li.q_fp8[tokens]), weights=np.ascontiguousarray(li.weights[tokens]),
+        cache=li.cache, block_table=np.ascontiguousarray(li.block_table[tokens]),
+        context_lens=np.ascontiguousarray(li.context_lens[tokens]), max_context=li.max_context)
+    err, out = oracle.mqa_logits(sub.q_fp8, sub.weights, sub.cache, sub.num_pages, sub.page_size,
+                                 sub.block_table, sub.context_lens, sub.max_context)
+    assert err == 0
+    return out
+
+
+def _check(li, tokens=None):
+    tokens = list(range(li.T)) if tokens is None else tokens
+    got = _run_gpu(li)[tokens]
+    ref = _oracle(li, tokens)
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isneginf(got), ~fin), "masked columns differ"
+    err = np.abs(got[fin].astype(np.float64) - ref[fin])
+    tol = _tolerance(li, tokens)[fin] + 1e-30
+    worst = float(np.max(err / tol)) if err.size else 0.0
+    assert np.all(err <= tol), f"max err/tol {worst}"
+    return worst
+
+
+@pytest.mark.parametrize("H", [16, 32, 64, 128])
+def test_small_ragged(H):
+    li = synth.make_logits(seed=H, T=3, H=H, context=300, ragged=True, spare_pages=2)
+    _check(li)
+
+
+def test_partial_tiles_and_empty_context():
+    li = synth.make_logits(seed=7, T=4, H=64, context=129)
+    li.context_lens = np.array([0, 1, 64, 129], np.int32)
+    li.max_context = 200
+    _check(li)
+
+
+def test_decode_full_size_sampled():
+    """64 sequences x 16384 keys x 64 heads (the decode step at 16K context);
+    every column of four tokens is checked against the oracle."""
+    li = synth.make_logits(seed=9, T=64, H=64, context=16384)
+    worst = _check(li, tokens=[0, 17, 40, 63])
+    print("max err/tol", worst)
+
+
+def test_bad_page_sets_error_bit():
+    li = synth.make_logits(seed=10, T=2, H=16, context=100)
+    li.block_table = li.block_table.copy()
+    li.block_table[1, 0] = li.num_pages + 5
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _run_gpu(li, err=err)
+    assert int(err.item()) & 2
+    ref = _oracle(li, [0])
+    fin = np.isfinite(ref)
+    assert np.all(np.abs(got[0][fin[0]] - ref[0][fin[0]]) <= _tolerance(li, [0])[0][fin[0]] + 1e-30)
