@@ -24,6 +24,8 @@ kernel launch.  Prints ONE JSON line (rank 0):
   unfused    the same call as four launches with bf16 intermediates (the
              pages' pre-fusion chain) on the prefill inputs and in the decode
              step, for the 4 -> 1 launch comparison
+  mqa_logits the indexer's fp8 paged MQA logits (the consumer of the index-K
+             cache) on the tcgen05 tensor cores at the 16K-context decode step
   cpu_baseline  the oracle (plain C, one core) on a bounded sample
 
 ``--impl reference`` times the oracle instead (the CPU statement of the path),
@@ -49,7 +51,8 @@ sys.path.insert(0, ROOT)
 METRIC = "tokens/s + achieved HBM GB/s (% of peak) prefill; µs/call at decode T=1..64"
 WORKLOAD = "prefill T=8192 H=64 D=128 rope_dim=64 NeoX, 128 pages x 64 (contiguous slots)"
 PROFILE = os.path.join(ROOT, "profiles", "dsa_pipeline_kernel_prefill_T8192_H64.md")
-KERNEL_SRC = os.path.join(ROOT, "prep_token_gb300", "csrc", "dsa_prep.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "prep_token_gb300", "csrc", f)
+               for f in ("dsa_prep.cu", "dsa_common.cuh")]
 L2_FLUSH_BYTES = 256 << 20
 GRAPH_STEPS = 50
 
@@ -80,6 +83,14 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
+def kernel_source_hash():
+    """sha256 over the sources the prefill kernel is compiled from."""
+    h = hashlib.sha256()
+    for f in KERNEL_SRCS:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
 def profile_traffic():
     """DRAM bytes per launch from the committed ncu summary, or None when the
     kernel source has changed since it was captured."""
@@ -90,7 +101,7 @@ def profile_traffic():
     m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
     if not (m_b and m_h):
         return None
-    cur = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+    cur = kernel_source_hash()
     return float(m_b.group(1)) if cur == m_h.group(1) else None
 
 
@@ -411,6 +422,10 @@ def run_ours(args, rank, world, local_rank):
                    "hbm_bytes_per_call": synth.algorithmic_bytes(T, H)
                    + T * (H + 1) * 128 * 2 * 2 + T * 128 * 2 * 2}
 
+    logits = None
+    if rank == 0 and not args.no_logits:
+        logits = _logits_timing(dp, torch, dev, peaks)
+
     decode = None
     if rank == 0 and not args.no_decode:
         decode = {"c2_decode_T64_H64_gptj": _decode_timings(
@@ -460,6 +475,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks.summary(),
         "decode": decode,
         "unfused": unfused,
+        "mqa_logits": logits,
         "cpu_baseline": cpu,
     }
 
@@ -541,6 +557,58 @@ def run_reference(args, rank, world):
     }
 
 
+def _logits_inputs(torch, dev, synth, T=64, H=64, context=16384):
+    li = synth.make_logits(seed=5, T=T, H=H, context=context)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    return li, dict(q=d(li.q_fp8), w=d(li.weights), cache=d(li.cache), bt=d(li.block_table),
+                    lens=d(li.context_lens),
+                    out=torch.empty((T, li.max_context), dtype=torch.float32, device=dev))
+
+
+def _logits_call(dp, li, t, stream):
+    dp.dsa_indexer_mqa_logits(t["q"], t["w"], t["cache"], li.page_size, t["bt"], t["lens"],
+                              li.max_context, logits=t["out"], stream=stream)
+
+
+def _logits_timing(dp, torch, dev, peaks, calls=10, reps=20):
+    """The indexer's fp8 paged MQA logits on the tensor cores, at the decode
+    step of the pages' serving bench (64 sequences, 16K context, 64 heads):
+    us per call, HBM GB/s and fp8 tensor TFLOP/s.  The 138 MB index-K cache is
+    larger than L2, so consecutive calls re-read it from HBM."""
+    import synth
+    li, t = _logits_inputs(torch, dev, synth)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            _logits_call(dp, li, t, stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            _logits_call(dp, li, t, stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / (calls * reps)
+    T, H, L = li.T, li.H, int(li.context_lens[0])
+    nbytes = T * (L * (128 + 4 + 4) + (L // 64) * 4 + H * (128 + 4) + 4)
+    flops = 2.0 * T * L * H * 128
+    fp8_peak = 2.0 * peaks.get("bf16_tflops", 1900.0)
+    return {"workload": f"T={T} H={H} context={L} page_size=64", "us_per_call": us,
+            "gb_per_s": nbytes / us / 1e3, "hbm_frac": nbytes / us / 1e3 / peaks["hbm_gbs"],
+            "tflops": flops / us / 1e6, "fp8_peak_tflops": fp8_peak,
+            "fp8_frac": flops / us / 1e6 / fp8_peak,
+            "peak_note": "fp8 peak = measured bf16 cuBLAS peak x 2 (the nominal fp8/bf16 ratio)",
+            "algorithmic_bytes": nbytes, "flops": flops, "calls": calls * reps,
+            "gpu_launches": calls * reps}
+
+
 def run_probe(which, local_rank):
     """A few eager calls on one workload, for ncu captures (no timing, no JSON)."""
     import torch
@@ -548,6 +616,13 @@ def run_probe(which, local_rank):
     import synth
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    if which == "logits":
+        li, t = _logits_inputs(torch, dev, synth)
+        for _ in range(6):
+            _logits_call(dp, li, t, torch.cuda.current_stream())
+        torch.cuda.synchronize(dev)
+        print(f"probe logits: 6 calls (T={li.T}, H={li.H}, context={li.max_context})")
+        return
     inp = synth.make_decode(seed=1) if which == "decode" else synth.make_prefill(seed=3)
     d = _dev_inputs(inp, dev)
     stream = torch.cuda.current_stream()
@@ -566,8 +641,9 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-unfused", action="store_true")
+    ap.add_argument("--no-logits", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--probe", choices=("prefill", "decode"),
+    ap.add_argument("--probe", choices=("prefill", "decode", "logits"),
                     help="make 6 eager calls on that workload and exit (for profilers)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -38,13 +38,29 @@ def _stale() -> bool:
 
 
 def build_library(force: bool = False, verbose: bool = False) -> str:
-    """Compile every .cu under csrc/ into one shared library (one nvcc call)."""
+    """Compile every .cu under csrc/ (in parallel, one nvcc per file) and
+    link them into one shared library."""
     if not force and not _stale():
         return LIB_PATH
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *NVCC_FLAGS, "-I", INCLUDE, "-o", tmp, *sources()]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.check_call(cmd)
-    os.replace(tmp, LIB_PATH)
+    tag = f"{os.getpid()}"
+    objs, procs = [], []
+    compile_flags = [f for f in NVCC_FLAGS if f not in ("-shared",)]
+    for src in sources():
+        obj = os.path.join(PKG, "csrc", os.path.basename(src) + f".{tag}.o")
+        cmd = [_nvcc(), *compile_flags, "-I", INCLUDE, "-c", "-o", obj, src]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        procs.append(subprocess.Popen(cmd))
+        objs.append(obj)
+    try:
+        codes = [p.wait() for p in procs]
+        if any(codes):
+            raise subprocess.CalledProcessError(max(codes), "nvcc -c")
+        tmp = LIB_PATH + f".tmp{tag}"
+        subprocess.check_call([_nvcc(), *NVCC_FLAGS, "-o", tmp, *objs])
+        os.replace(tmp, LIB_PATH)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return LIB_PATH
