@@ -292,18 +292,23 @@ __global__ void __launch_bounds__(kLThreads, 1)
     const int sub = warp & 3;               // the TMEM lanes this warp may read
     const int row = 32 * sub + lane;        // key within the tile
     float* out = p.logits + static_cast<long long>(t) * p.logits_stride;
+    // the key scale of this thread's key in tile i (0 past the context)
+    auto key_scale = [&](int i) {
+      const int j = i * kTileKeys + row;
+      if (i >= ntiles || j >= len) return 0.0f;
+      long long pg = __ldg(p.block_table + t * p.bt_stride + j / kPageKeys);
+      if (pg < 0 || pg >= p.num_pages) pg = 0;
+      return __ldg(reinterpret_cast<const float*>(p.cache + pg * kPageStride + kPageBytes) +
+                   (j % kPageKeys));
+    };
     int m = 0;
     bool ok = true;
+    float ks_next = key_scale(blockIdx.x);
     for (int i = blockIdx.x; i < p.tiles_max; i += gridDim.x) {
       const int j = i * kTileKeys + row;
       if (i < ntiles && ok) {
-        float ks = 0.0f;
-        if (j < len) {
-          long long pg = __ldg(p.block_table + t * p.bt_stride + j / kPageKeys);
-          if (pg < 0 || pg >= p.num_pages) pg = 0;
-          ks = __ldg(reinterpret_cast<const float*>(p.cache + pg * kPageStride + kPageBytes) +
-                     (j % kPageKeys));
-        }
+        const float ks = ks_next;
+        ks_next = key_scale(i + gridDim.x);   // in flight while this tile is reduced
         const int b = m & 1;
         const bool got = mbar_wait(accfull(b), (m >> 1) & 1, abort_flag);
         if (!__all_sync(kFull, got)) {
@@ -369,6 +374,7 @@ using LogitsFn = void (*)(CUtensorMap, CUtensorMap, LParams);
 
 struct LDevice {
   int sms = 0;
+  int occ[4] = {1, 1, 1, 1};  // resident CTAs per SM for H = 16, 32, 64, 128
   bool ready = false;
 };
 constexpr int kMaxLDevices = 64;
@@ -376,9 +382,15 @@ LDevice g_ldev[kMaxLDevices];
 std::mutex g_ldev_mu;
 
 template <int NH>
-cudaError_t prepare_kernel() {
-  return cudaFuncSetAttribute(dsa_mqa_logits_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              LSmem<NH>::kBytes + 1024);
+cudaError_t prepare_kernel(int* occ) {
+  cudaError_t e = cudaFuncSetAttribute(dsa_mqa_logits_kernel<NH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       LSmem<NH>::kBytes + 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, dsa_mqa_logits_kernel<NH>, kLThreads,
+                                                    LSmem<NH>::kBytes + 1024);
+  if (e == cudaSuccess && *occ < 1) *occ = 1;
+  return e;
 }
 
 cudaError_t logits_device(int* sms) {
@@ -390,15 +402,22 @@ cudaError_t logits_device(int* sms) {
   LDevice& d = g_ldev[dev];
   if (!d.ready) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = prepare_kernel<16>();
-    if (e == cudaSuccess) e = prepare_kernel<32>();
-    if (e == cudaSuccess) e = prepare_kernel<64>();
-    if (e == cudaSuccess) e = prepare_kernel<128>();
+    if (e == cudaSuccess) e = prepare_kernel<16>(&d.occ[0]);
+    if (e == cudaSuccess) e = prepare_kernel<32>(&d.occ[1]);
+    if (e == cudaSuccess) e = prepare_kernel<64>(&d.occ[2]);
+    if (e == cudaSuccess) e = prepare_kernel<128>(&d.occ[3]);
     if (e != cudaSuccess) return e;
     d.ready = true;
   }
   *sms = d.sms;
   return cudaSuccess;
+}
+
+int resident_ctas(int H) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxLDevices) return 1;
+  const int i = H == 16 ? 0 : H == 32 ? 1 : H == 64 ? 2 : 3;
+  return g_ldev[dev].sms * g_ldev[dev].occ[i];
 }
 
 template <int NH>
@@ -492,8 +511,9 @@ dsa_status dsa_indexer_mqa_logits(const void* q_fp8, const float* weights,
   p.tiles_max = (max_context + kTileKeys - 1) / kTileKeys;
   p.T = T;
   p.err = err_flags;
-  // split each token's tiles over enough CTAs to cover the SMs twice
-  int gx = (2 * sms + T - 1) / T;
+  // split each token's tiles over as many CTAs as fit on the GPU at once
+  // (all resident: no second wave), at least one per token
+  int gx = resident_ctas(H) / T;
   if (gx > p.tiles_max) gx = p.tiles_max;
   if (gx < 1) gx = 1;
   const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(T));
