@@ -381,16 +381,35 @@ constexpr int kMaxLDevices = 64;
 LDevice g_ldev[kMaxLDevices];
 std::mutex g_ldev_mu;
 
+// Resident CTAs per SM, from the limits that bind here: shared memory (with
+// the per-block reservation), registers and threads.
 template <int NH>
-cudaError_t prepare_kernel(int* occ) {
+cudaError_t prepare_kernel(int dev, int* occ) {
+  const int smem = LSmem<NH>::kBytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(dsa_mqa_logits_kernel<NH>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       LSmem<NH>::kBytes + 1024);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(dsa_mqa_logits_kernel<NH>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  cudaFuncAttributes fa;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, dsa_mqa_logits_kernel<NH>);
+  int sm_smem = 0, reserved = 0, sm_regs = 0, sm_threads = 0;
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&sm_threads, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
   if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, dsa_mqa_logits_kernel<NH>, kLThreads,
-                                                    LSmem<NH>::kBytes + 1024);
-  if (e == cudaSuccess && *occ < 1) *occ = 1;
-  return e;
+  int n = sm_smem / (smem + reserved);
+  const int by_regs = sm_regs / (kLThreads * (fa.numRegs > 0 ? fa.numRegs : 1));
+  const int by_threads = sm_threads / kLThreads;
+  if (by_regs < n) n = by_regs;
+  if (by_threads < n) n = by_threads;
+  *occ = n < 1 ? 1 : n;
+  return cudaSuccess;
 }
 
 cudaError_t logits_device(int* sms) {
@@ -402,10 +421,10 @@ cudaError_t logits_device(int* sms) {
   LDevice& d = g_ldev[dev];
   if (!d.ready) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = prepare_kernel<16>(&d.occ[0]);
-    if (e == cudaSuccess) e = prepare_kernel<32>(&d.occ[1]);
-    if (e == cudaSuccess) e = prepare_kernel<64>(&d.occ[2]);
-    if (e == cudaSuccess) e = prepare_kernel<128>(&d.occ[3]);
+    if (e == cudaSuccess) e = prepare_kernel<16>(dev, &d.occ[0]);
+    if (e == cudaSuccess) e = prepare_kernel<32>(dev, &d.occ[1]);
+    if (e == cudaSuccess) e = prepare_kernel<64>(dev, &d.occ[2]);
+    if (e == cudaSuccess) e = prepare_kernel<128>(dev, &d.occ[3]);
     if (e != cudaSuccess) return e;
     d.ready = true;
   }
