@@ -13,7 +13,9 @@ Kernel-level evidence), plus the OCP OFP8 spec for the E4M3 format.
 
 Parity unpinned (stated readings, no pin from the pages): the 1e-4 amax
 floor of the scale, the constants folded into the gate weights
-(softmax_scale * H^-0.5) and the order LayerNorm-then-RoPE on k.
+(softmax_scale * H^-0.5) and the order LayerNorm-then-RoPE on k.  The
+Hadamard rotation (``hadamard``) is pinned to the Sylvester matrix of scipy
+and to a float64 brute force of the rotated pipeline.
 """
 from __future__ import annotations
 
@@ -70,6 +72,10 @@ def _load():
         lib.oracle_qk_prepare_store.restype = ctypes.c_int
         lib.oracle_qk_prepare_store_chain.argtypes = lib.oracle_qk_prepare_store.argtypes
         lib.oracle_qk_prepare_store_chain.restype = ctypes.c_int
+        lib.oracle_qk_prepare_store_hadamard.argtypes = lib.oracle_qk_prepare_store.argtypes
+        lib.oracle_qk_prepare_store_hadamard.restype = ctypes.c_int
+        lib.oracle_hadamard.argtypes = [P]
+        lib.oracle_hadamard.restype = None
         lib.oracle_mqa_logits.argtypes = [I32, I32, P, P, P, I64, I32, P, I64, P, P, I64, I32]
         lib.oracle_mqa_logits.restype = ctypes.c_int
         _lib = lib
@@ -124,6 +130,15 @@ def ue8m0_exponent(amax) -> np.ndarray:
     for i, x in enumerate(flat.tolist()):
         out[i] = lib.oracle_ue8m0_exponent(x)
     return out.reshape(a.shape)
+
+
+def hadamard(x) -> np.ndarray:
+    """Rows of x ([n, 128] fp32) -> H_128 x / sqrt(128), fp32 butterflies."""
+    lib = _load()
+    y = np.array(x, dtype=np.float32, copy=True, order="C").reshape(-1, 128)
+    for i in range(y.shape[0]):
+        lib.oracle_hadamard(_ptr(y[i]))
+    return y
 
 
 def layernorm(x, gamma, beta, eps: float) -> np.ndarray:
@@ -188,12 +203,13 @@ def qk_prepare_store(q, q_stride_t, q_stride_h, k, k_stride_t, w, w_stride_t,
                      positions, slots, cos_t, sin_t, cs_stride, max_position,
                      gamma, beta, eps, softmax_scale, q_fp8, weights, cache,
                      num_pages, page_size, H, rope_dim, style, T=None, chain=False,
-                     token_major=False):
+                     token_major=False, hadamard=False):
     """Fused Q/K prepare-and-store.  q/k/w are bf16 bit patterns (uint16)
     with the given strides in elements.  ``q_fp8`` ([T, H, 128] uint8),
     ``weights`` ([T, H] fp32) and ``cache`` (uint8) are written in place.
     ``chain=True`` gives the outputs of the four-launch unfused chain, which
-    rounds the LayerNorm output and the rotated vectors to bf16.
+    rounds the LayerNorm output and the rotated vectors to bf16;
+    ``hadamard=True`` rotates q heads and k by H_128 / sqrt(128) after RoPE.
     Returns (err_bits, q_scale_exp[T, H], k_scale_exp[T])."""
     lib = _load()
     positions = _req(positions, np.int64)
@@ -209,7 +225,10 @@ def qk_prepare_store(q, q_stride_t, q_stride_h, k, k_stride_t, w, w_stride_t,
         raise ValueError("output buffers too small")
     qe = np.zeros((max(T, 1), H), np.int32)
     ke = np.zeros(max(T, 1), np.int32)
-    fn = lib.oracle_qk_prepare_store_chain if chain else lib.oracle_qk_prepare_store
+    if chain and hadamard:
+        raise ValueError("the chain has no Hadamard variant")
+    fn = lib.oracle_qk_prepare_store_chain if chain else (
+        lib.oracle_qk_prepare_store_hadamard if hadamard else lib.oracle_qk_prepare_store)
     err = fn(
         T, H, _ptr(q), q_stride_t, q_stride_h, _ptr(k), k_stride_t, _ptr(w), w_stride_t,
         _ptr(positions), _ptr(slots), _ptr(cos_t), _ptr(sin_t), cs_stride, max_position,

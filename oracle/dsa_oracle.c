@@ -38,6 +38,11 @@
  *   - index-K cache page p holds page_size*128 code bytes, then page_size
  *     fp32 scales; slot s lives in page s / page_size at offset s % page_size
  *     (the other layout: 132 bytes per slot, codes then scale).
+ *   - The Hadamard variant (the rotation [FUSE-QK] Modifications says the
+ *     fused path leaves out): after RoPE, each q head and k is multiplied by
+ *     the Sylvester matrix H_128 divided by sqrt(128); computed as fp32
+ *     butterflies over index bits 0..6 in that order, then one multiply by
+ *     fp32(128^-0.5), so every rounding is fixed.
  *
  * Build: plain C99, -O2 -ffp-contract=off (no fused multiply-add except the
  * explicit fmaf calls the RoPE form asks for).
@@ -155,6 +160,25 @@ void oracle_rope(float* x, const float* cos_row, const float* sin_row,
   }
 }
 
+/* The Hadamard rotation that [FUSE-QK] Modifications says the fused path
+ * assumes absent ("the no-Hadamard invariant"): x <- H_128 x / sqrt(128), the
+ * normalised Walsh-Hadamard transform, applied after RoPE and before the
+ * quantiser.  Written as the radix-2 butterfly network in fp32, stage by stage
+ * over index bits 0, 1, ..., 6 -- each stage replaces (a, b) = (x[i], x[i+h])
+ * by (a + b, a - b) for every i with bit h clear -- and then one multiply by
+ * the fp32 value of 128^-0.5; that fixes every rounding. */
+void oracle_hadamard(float* x) {
+  for (int h = 1; h < DSA_D; h <<= 1)
+    for (int i = 0; i < DSA_D; ++i)
+      if ((i & h) == 0) {
+        float a = x[i], b = x[i + h];
+        x[i] = a + b;
+        x[i + h] = a - b;
+      }
+  const float s = (float)(1.0 / sqrt((double)DSA_D));
+  for (int i = 0; i < DSA_D; ++i) x[i] = x[i] * s;
+}
+
 /* [FUSE-Q] "q -> FP8 (ue8m0) quant"; [FUSE-QK] Accuracy (fp32 -> fp8 in one
  * step): one power-of-two scale per 128-vector, codes = e4m3(z / scale).
  * Returns the scale exponent e. */
@@ -200,13 +224,14 @@ static void store_index_k(uint8_t* cache, int64_t slot, int32_t page_size,
 static int prepare_k(const uint16_t* krow, const float* cos_row,
                      const float* sin_row, const float* gamma,
                      const float* beta, float eps, int rope_dim, int style,
-                     int bf16_intermediate, uint8_t* codes) {
+                     int bf16_intermediate, int hadamard, uint8_t* codes) {
   float x[DSA_D], y[DSA_D];
   for (int j = 0; j < DSA_D; ++j) x[j] = bf16_to_f32(krow[j]);
   oracle_layernorm(x, gamma, beta, eps, y);
   if (bf16_intermediate == 2)
     for (int j = 0; j < DSA_D; ++j) y[j] = round_to_bf16(y[j]);
   oracle_rope(y, cos_row, sin_row, rope_dim, style);
+  if (hadamard) oracle_hadamard(y);
   if (bf16_intermediate)
     for (int j = 0; j < DSA_D; ++j) y[j] = round_to_bf16(y[j]);
   return oracle_quantize_vector(y, codes);
@@ -217,7 +242,7 @@ static int prepare_k(const uint16_t* krow, const float* cos_row,
  * error bits: 1 = a position outside [0, max_position) (token skipped),
  * 2 = a slot outside [0, num_pages * page_size) (cache write skipped).
  * k_scale_exp, if not NULL, receives each token's scale exponent. */
-int oracle_k_prepare_store(int64_t T, const uint16_t* k, int64_t k_stride_t,
+static int k_prepare_store(int64_t T, const uint16_t* k, int64_t k_stride_t,
                            const int64_t* positions, const int64_t* slots,
                            const float* cos_t, const float* sin_t,
                            int64_t cs_stride, int64_t max_position,
@@ -225,7 +250,7 @@ int oracle_k_prepare_store(int64_t T, const uint16_t* k, int64_t k_stride_t,
                            uint8_t* cache, int64_t num_pages, int32_t page_size,
                            int32_t rope_dim, int32_t style,
                            int32_t bf16_intermediate, int32_t* k_scale_exp,
-                           int32_t token_major) {
+                           int32_t token_major, int32_t hadamard) {
   int err = 0;
   for (int64_t t = 0; t < T; ++t) {
     int64_t pos = positions[t];
@@ -236,7 +261,7 @@ int oracle_k_prepare_store(int64_t T, const uint16_t* k, int64_t k_stride_t,
     uint8_t codes[DSA_D];
     int e = prepare_k(k + t * k_stride_t, cos_t + pos * cs_stride,
                       sin_t + pos * cs_stride, gamma, beta, eps, rope_dim,
-                      style, bf16_intermediate, codes);
+                      style, bf16_intermediate, hadamard, codes);
     if (k_scale_exp) k_scale_exp[t] = e;
     int64_t slot = slots[t];
     if (slot < 0 || slot >= num_pages * (int64_t)page_size) {
@@ -248,8 +273,23 @@ int oracle_k_prepare_store(int64_t T, const uint16_t* k, int64_t k_stride_t,
   return err;
 }
 
+int oracle_k_prepare_store(int64_t T, const uint16_t* k, int64_t k_stride_t,
+                           const int64_t* positions, const int64_t* slots,
+                           const float* cos_t, const float* sin_t,
+                           int64_t cs_stride, int64_t max_position,
+                           const float* gamma, const float* beta, float eps,
+                           uint8_t* cache, int64_t num_pages, int32_t page_size,
+                           int32_t rope_dim, int32_t style,
+                           int32_t bf16_intermediate, int32_t* k_scale_exp,
+                           int32_t token_major) {
+  return k_prepare_store(T, k, k_stride_t, positions, slots, cos_t, sin_t, cs_stride,
+                         max_position, gamma, beta, eps, cache, num_pages, page_size,
+                         rope_dim, style, bf16_intermediate, k_scale_exp, token_major, 0);
+}
+
 /* Both Q/K writers; chain != 0 rounds the tensors the four-launch chain
- * hands between launches to bf16 (see prepare_k). */
+ * hands between launches to bf16 (see prepare_k); hadamard != 0 rotates
+ * every rotated q head and k by oracle_hadamard before quantising. */
 static int qk_prepare_store(
     int64_t T, int32_t H, const uint16_t* q, int64_t q_stride_t,
     int64_t q_stride_h, const uint16_t* k, int64_t k_stride_t,
@@ -259,7 +299,7 @@ static int qk_prepare_store(
     const float* beta, float eps, float softmax_scale, uint8_t* q_fp8,
     float* weights, uint8_t* cache, int64_t num_pages, int32_t page_size,
     int32_t rope_dim, int32_t style, int32_t* q_scale_exp,
-    int32_t* k_scale_exp, int chain, int32_t token_major) {
+    int32_t* k_scale_exp, int chain, int32_t token_major, int hadamard) {
   int err = 0;
   double head_factor = 1.0 / sqrt((double)H);
   for (int64_t t = 0; t < T; ++t) {
@@ -275,6 +315,7 @@ static int qk_prepare_store(
       float z[DSA_D];
       for (int j = 0; j < DSA_D; ++j) z[j] = bf16_to_f32(qrow[j]);
       oracle_rope(z, cos_row, sin_row, rope_dim, style);
+      if (hadamard) oracle_hadamard(z);
       if (chain)
         for (int j = 0; j < DSA_D; ++j) z[j] = round_to_bf16(z[j]);
       int e = oracle_quantize_vector(z, q_fp8 + (t * H + h) * DSA_D);
@@ -283,12 +324,12 @@ static int qk_prepare_store(
       weights[t * H + h] =
           (float)(wv * ldexp(1.0, e) * (double)softmax_scale * head_factor);
     }
-    err |= oracle_k_prepare_store(1, k + t * k_stride_t, k_stride_t,
-                                  positions + t, slots + t, cos_t, sin_t,
-                                  cs_stride, max_position, gamma, beta, eps,
-                                  cache, num_pages, page_size, rope_dim, style,
-                                  chain ? 2 : 0, k_scale_exp ? k_scale_exp + t : NULL,
-                                  token_major);
+    err |= k_prepare_store(1, k + t * k_stride_t, k_stride_t,
+                           positions + t, slots + t, cos_t, sin_t,
+                           cs_stride, max_position, gamma, beta, eps,
+                           cache, num_pages, page_size, rope_dim, style,
+                           chain ? 2 : 0, k_scale_exp ? k_scale_exp + t : NULL,
+                           token_major, hadamard);
   }
   return err;
 }
@@ -312,7 +353,7 @@ int oracle_qk_prepare_store(
                           w_stride_t, positions, slots, cos_t, sin_t, cs_stride,
                           max_position, gamma, beta, eps, softmax_scale, q_fp8,
                           weights, cache, num_pages, page_size, rope_dim, style,
-                          q_scale_exp, k_scale_exp, 0, token_major);
+                          q_scale_exp, k_scale_exp, 0, token_major, 0);
 }
 
 /* The same outputs as written by the four-launch chain of [FUSE-QK] Profile,
@@ -332,7 +373,27 @@ int oracle_qk_prepare_store_chain(
                           w_stride_t, positions, slots, cos_t, sin_t, cs_stride,
                           max_position, gamma, beta, eps, softmax_scale, q_fp8,
                           weights, cache, num_pages, page_size, rope_dim, style,
-                          q_scale_exp, k_scale_exp, 1, token_major);
+                          q_scale_exp, k_scale_exp, 1, token_major, 0);
+}
+
+/* The Q/K writer with the Hadamard rotation (see oracle_hadamard): every
+ * rotated q head and the normalised, rotated k pass through H_128 / sqrt(128)
+ * before they are quantised. */
+int oracle_qk_prepare_store_hadamard(
+    int64_t T, int32_t H, const uint16_t* q, int64_t q_stride_t,
+    int64_t q_stride_h, const uint16_t* k, int64_t k_stride_t,
+    const uint16_t* w, int64_t w_stride_t, const int64_t* positions,
+    const int64_t* slots, const float* cos_t, const float* sin_t,
+    int64_t cs_stride, int64_t max_position, const float* gamma,
+    const float* beta, float eps, float softmax_scale, uint8_t* q_fp8,
+    float* weights, uint8_t* cache, int64_t num_pages, int32_t page_size,
+    int32_t rope_dim, int32_t style, int32_t* q_scale_exp,
+    int32_t* k_scale_exp, int32_t token_major) {
+  return qk_prepare_store(T, H, q, q_stride_t, q_stride_h, k, k_stride_t, w,
+                          w_stride_t, positions, slots, cos_t, sin_t, cs_stride,
+                          max_position, gamma, beta, eps, softmax_scale, q_fp8,
+                          weights, cache, num_pages, page_size, rope_dim, style,
+                          q_scale_exp, k_scale_exp, 0, token_major, 1);
 }
 
 /* ------------------------------------------------------------ the consumer */

@@ -21,7 +21,7 @@ def fresh_cache(inp, fill=SENTINEL):
     return np.full(inp.cache_bytes, fill, np.uint8)
 
 
-def run_oracle_qk(inp, cache=None, T=None, chain=False):
+def run_oracle_qk(inp, cache=None, T=None, chain=False, hadamard=False):
     T = inp.T if T is None else T
     cache = fresh_cache(inp) if cache is None else cache
     q_fp8 = np.zeros((max(T, 1), inp.H, 128), np.uint8)
@@ -36,7 +36,7 @@ def run_oracle_qk(inp, cache=None, T=None, chain=False):
         inp.positions[:T], inp.slots[:T], inp.cos, inp.sin, inp.cs_stride,
         inp.max_position, inp.gamma, inp.beta, inp.eps, inp.softmax_scale,
         q_fp8, weights, cache, inp.num_pages, inp.page_size, inp.H, inp.rope_dim,
-        inp.style, T=T, chain=chain, token_major=inp.token_major)
+        inp.style, T=T, chain=chain, token_major=inp.token_major, hadamard=hadamard)
     return dict(q_fp8=q_fp8[:T], weights=weights[:T], cache=cache, err=err,
                 q_exp=qe, k_exp=ke)
 

@@ -311,3 +311,28 @@ def test_layouts_hold_the_same_slots(page_size):
         assert np.array_equal(ts[inp.slots], ps[inp.slots])
         assert np.array_equal(tm["q_fp8"], paged["q_fp8"])
     assert np.all((ts[inp.slots].view(np.uint32) & 0x7FFFFF) == 0)
+
+
+@pytest.mark.parametrize("style", [synth.NEOX, synth.GPTJ])
+def test_hadamard_variant_bruteforce_tiny(style):
+    """The Hadamard variant against float64: RoPE, then the orthonormal
+    Walsh-Hadamard rotation, then the usual quantiser."""
+    from scipy.linalg import hadamard as sylvester
+    from _brute import bf16, quant64, rope64
+    Hm = sylvester(128) / np.sqrt(128.0)
+    inp = synth.make_tiny(seed=13, T=3, H=2, style=style, fused_kw=True)
+    out = run_oracle_qk(inp, hadamard=True)
+    codes, _ = cache_views(inp, out["cache"])
+    for t in range(inp.T):
+        p = inp.positions[t]
+        for h in range(inp.H):
+            z = Hm @ rope64(bf16(inp.q[t, h]), inp.cos[p], inp.sin[p], 64, style)
+            qc, qe = quant64(z)
+            assert qe == out["q_exp"][t, h]
+            assert code_distance(out["q_fp8"][t, h], qc).max() <= 1
+        x = bf16(inp.kw[t, :128])
+        y = (x - x.mean()) / np.sqrt(((x - x.mean()) ** 2).mean() + float(np.float32(inp.eps)))
+        y = y * inp.gamma + inp.beta
+        kc, ke = quant64(Hm @ rope64(y, inp.cos[p], inp.sin[p], 64, style))
+        assert ke == out["k_exp"][t]
+        assert code_distance(codes[inp.slots[t]], kc).max() <= 1

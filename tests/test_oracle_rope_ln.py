@@ -146,3 +146,26 @@ def test_layernorm_matches_torch_float64():
         torch.from_numpy(beta).double(), eps=1e-6).float().numpy()
     ulp = np.spacing(np.abs(ref))
     assert np.all(np.abs(y - ref) <= ulp)
+
+
+def test_hadamard_matches_scipy_and_is_an_involution():
+    from scipy.linalg import hadamard as sylvester
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal((64, 128)) * 5).astype(np.float32)
+    y = oracle.hadamard(x)
+    ref = x.astype(np.float64) @ sylvester(128).T / np.sqrt(128.0)
+    scale = np.abs(x).sum(axis=1, keepdims=True) / np.sqrt(128.0)
+    assert np.all(np.abs(y - ref) <= 8 * 2.0 ** -24 * scale)
+    # orthonormal and symmetric: applying it twice gives x back, norms are kept
+    assert np.allclose(oracle.hadamard(y), x, rtol=0, atol=1e-5 * np.abs(x).max())
+    assert np.allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-6)
+
+
+def test_hadamard_of_unit_vectors():
+    """H e_j / sqrt(128) is the j-th Sylvester column scaled: entries +-2^-3.5."""
+    x = np.eye(128, dtype=np.float32)[[0, 1, 77]]
+    y = oracle.hadamard(x)
+    s = np.float32(1.0 / np.sqrt(128.0))
+    assert np.all(np.abs(y) == s)
+    assert np.all(y[0] == s)
+    assert np.array_equal(y[1], np.where(np.arange(128) & 1, -s, s).astype(np.float32))
