@@ -21,6 +21,8 @@ kernel launch.  Prints ONE JSON line (rank 0):
              q, k|w, outputs and index-K cache) captured as a CUDA graph and
              replayed after an L2 flush -- plain, with PDL, and with PDL plus
              early rope reads -- plus a single-call graph and eager calls
+  hadamard   the Hadamard-rotated variant (q and k times H_128 / sqrt(128)
+             after RoPE) on the prefill inputs and in the decode step
   unfused    the same call as four launches with bf16 intermediates (the
              pages' pre-fusion chain) on the prefill inputs and in the decode
              step, for the 4 -> 1 launch comparison
@@ -52,7 +54,7 @@ METRIC = "tokens/s + achieved HBM GB/s (% of peak) prefill; µs/call at decode T
 WORKLOAD = "prefill T=8192 H=64 D=128 rope_dim=64 NeoX, 128 pages x 64 (contiguous slots)"
 PROFILE = os.path.join(ROOT, "profiles", "dsa_pipeline_kernel_prefill_T8192_H64.md")
 KERNEL_SRCS = [os.path.join(ROOT, "prep_token_gb300", "csrc", f)
-               for f in ("dsa_prep.cu", "dsa_common.cuh")]
+               for f in ("dsa_prep.cu", "dsa_prep_kernels.cuh", "dsa_common.cuh")]
 L2_FLUSH_BYTES = 256 << 20
 GRAPH_STEPS = 50
 
@@ -192,7 +194,7 @@ def _add_workspace(dp, torch, inp, d, dev):
                           device=dev)
 
 
-def _call(dp, inp, d, stream, T=None, k_only=False, pdl=False, unfused=False):
+def _call(dp, inp, d, stream, T=None, k_only=False, pdl=False, unfused=False, hadamard=False):
     if unfused:
         dp.dsa_indexer_qk_prepare_store_unfused(
             d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
@@ -204,17 +206,43 @@ def _call(dp, inp, d, stream, T=None, k_only=False, pdl=False, unfused=False):
         dp.dsa_indexer_k_prepare_store(
             d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
             inp.eps, d["cache"], inp.page_size, inp.rope_dim, inp.style,
-            max_position=inp.max_position, stream=stream, num_tokens=T, pdl=pdl)
+            max_position=inp.max_position, stream=stream, num_tokens=T, pdl=pdl,
+            hadamard=hadamard)
         return
     dp.dsa_indexer_qk_prepare_store(
         d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
         d["beta"], inp.eps, inp.softmax_scale, d["cache"], inp.page_size, inp.rope_dim,
         inp.style, q_fp8_out=d["q_out"], weights_out=d["w_out"],
-        max_position=inp.max_position, stream=stream, num_tokens=T, pdl=pdl)
+        max_position=inp.max_position, stream=stream, num_tokens=T, pdl=pdl, hadamard=hadamard)
+
+
+def _prefill_graph_us(torch, sets, stream, call, steps):
+    """us per call of `call(inp, d)` on the alternating prefill sets: a graph
+    of 10 calls replayed up to 100 times (after 3 eager warm-up calls)."""
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            call(*sets[i & 1])
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(10):
+            call(*sets[i & 1])
+    reps = max(1, min(100, steps // 10))
+    with torch.cuda.stream(stream):
+        g.replay()
+        u0 = torch.cuda.Event(enable_timing=True)
+        u1 = torch.cuda.Event(enable_timing=True)
+        u0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        u1.record(stream)
+    stream.synchronize()
+    del g
+    return u0.elapsed_time(u1) * 1000.0 / (10 * reps), 10 * reps
 
 
 def _decode_timings(dp, torch, dev, make, reps=30, layers=21, k_only_too=False,
-                    unfused_too=False):
+                    unfused_too=False, hadamard=False):
     """us per call for one decode step of `layers` indexer layers: the layers
     share the step's positions, slots and rope cache (as in a model) and each
     has its own q, k|w, outputs and index-K cache.  Timed as a graph of the
@@ -245,7 +273,7 @@ def _decode_timings(dp, torch, dev, make, reps=30, layers=21, k_only_too=False,
     for name, k_only, unfused in modes:
         with torch.cuda.stream(stream):
             for inp, d in sets:          # warm-up outside capture
-                _call(dp, inp, d, stream, k_only=k_only, unfused=unfused)
+                _call(dp, inp, d, stream, k_only=k_only, unfused=unfused, hadamard=hadamard)
         stream.synchronize()
         res = {"launches_per_call": 4 if unfused else 1}
         variants = ((layers, False, f"graph{layers}_us"), (layers, True, f"graph{layers}_pdl_us"))
@@ -255,7 +283,8 @@ def _decode_timings(dp, torch, dev, make, reps=30, layers=21, k_only_too=False,
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for inp, d in sets[:n_layers]:
-                    _call(dp, inp, d, stream, k_only=k_only, pdl=pdl, unfused=unfused)
+                    _call(dp, inp, d, stream, k_only=k_only, pdl=pdl, unfused=unfused,
+                          hadamard=hadamard)
             times = []
             for _ in range(reps):
                 with torch.cuda.stream(stream):
@@ -278,7 +307,7 @@ def _decode_timings(dp, torch, dev, make, reps=30, layers=21, k_only_too=False,
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 for inp, d in sets:
-                    _call(dp, inp, d, stream, k_only=k_only, unfused=unfused)
+                    _call(dp, inp, d, stream, k_only=k_only, unfused=unfused, hadamard=hadamard)
                 e1.record(stream)
                 stream.synchronize()
                 times.append(e0.elapsed_time(e1) * 1000.0 / len(sets))
@@ -395,32 +424,29 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_unfused:
         for inp, d in sets:
             _add_workspace(dp, torch, inp, d, dev)
-        with torch.cuda.stream(stream):
-            for i in range(3):
-                _call(dp, sets[i & 1][0], sets[i & 1][1], stream, unfused=True)
-        stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(10):
-                _call(dp, sets[i & 1][0], sets[i & 1][1], stream, unfused=True)
-        reps = max(1, min(100, args.steps // 10))
-        with torch.cuda.stream(stream):
-            g.replay()
-            u0 = torch.cuda.Event(enable_timing=True)
-            u1 = torch.cuda.Event(enable_timing=True)
-            u0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            u1.record(stream)
-        stream.synchronize()
-        del g
-        uus = u0.elapsed_time(u1) * 1000.0 / (10 * reps)
+        uus, ucalls = _prefill_graph_us(
+            torch, sets, stream, lambda inp, d: _call(dp, inp, d, stream, unfused=True),
+            args.steps)
         for _, d in sets:
             del d["ws"]
-        unfused = {"prefill_us": uus, "launches_per_call": 4, "calls": 10 * reps,
+        unfused = {"prefill_us": uus, "launches_per_call": 4, "calls": ucalls,
                    "fused_speedup": uus / launch_us,
                    "hbm_bytes_per_call": synth.algorithmic_bytes(T, H)
                    + T * (H + 1) * 128 * 2 * 2 + T * 128 * 2 * 2}
+
+    # the Hadamard-rotated variant: same bytes, more arithmetic per vector
+    hadamard = None
+    if not args.no_hadamard:
+        hus, hcalls = _prefill_graph_us(
+            torch, sets, stream, lambda inp, d: _call(dp, inp, d, stream, hadamard=True),
+            args.steps)
+        hgb = algo_bytes / (hus * 1e-6) / 1e9
+        hadamard = {"prefill_us": hus, "calls": hcalls, "gb_per_s": hgb,
+                    "hbm_frac": hgb / peaks["hbm_gbs"], "tokens_per_s": T / (hus * 1e-6),
+                    "vs_plain": hus / launch_us, "launches_per_call": 1}
+        if rank == 0 and not args.no_decode:
+            hadamard["c2_decode_T64_H64_gptj"] = _decode_timings(
+                dp, torch, dev, lambda i: synth.make_decode(seed=1 + 100 * i), hadamard=True)
 
     logits = None
     if rank == 0 and not args.no_logits:
@@ -475,6 +501,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks.summary(),
         "decode": decode,
         "unfused": unfused,
+        "hadamard": hadamard,
         "mqa_logits": logits,
         "cpu_baseline": cpu,
     }
@@ -623,11 +650,12 @@ def run_probe(which, local_rank):
         torch.cuda.synchronize(dev)
         print(f"probe logits: 6 calls (T={li.T}, H={li.H}, context={li.max_context})")
         return
-    inp = synth.make_decode(seed=1) if which == "decode" else synth.make_prefill(seed=3)
+    had = which.endswith("_hadamard")
+    inp = synth.make_decode(seed=1) if which.startswith("decode") else synth.make_prefill(seed=3)
     d = _dev_inputs(inp, dev)
     stream = torch.cuda.current_stream()
     for _ in range(6):
-        _call(dp, inp, d, stream)
+        _call(dp, inp, d, stream, hadamard=had)
     torch.cuda.synchronize(dev)
     print(f"probe {which}: 6 calls (T={inp.T}, H={inp.H})")
 
@@ -642,8 +670,10 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-unfused", action="store_true")
     ap.add_argument("--no-logits", action="store_true")
+    ap.add_argument("--no-hadamard", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--probe", choices=("prefill", "decode", "logits"),
+    ap.add_argument("--probe", choices=("prefill", "decode", "logits", "prefill_hadamard",
+                                        "decode_hadamard"),
                     help="make 6 eager calls on that workload and exit (for profilers)")
     args = ap.parse_args()
     if args.warmup < 3:

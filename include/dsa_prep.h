@@ -119,6 +119,18 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
  * then its fp32 scale -- and page_size only sets the slot count
  * num_pages * page_size.  Same buffer size either way. */
 #define DSA_FLAG_CACHE_TOKEN_MAJOR 16u
+/* Hadamard-rotated variant.  After RoPE (and, for k, LayerNorm then RoPE)
+ * every q head and k is multiplied by H_128 / sqrt(128), H_128 the Sylvester
+ * Walsh-Hadamard matrix, before its scale and codes are taken -- the rotation
+ * that the fused path of sglang PR "[AMD] [GLM5] Fuse the DSA indexer Q/K
+ * rope + quant + K-cache write" (Modifications, "no-Hadamard invariant")
+ * leaves out.  The product is computed as fp32 butterflies over index bits
+ * 0, 1, ..., 6 in that order, (a, b) -> (a + b, a - b), then one multiply by
+ * fp32(128^-0.5): the rounding is fixed, so the codes are reproducible.
+ * Scores are unchanged up to quantisation, since H_128 / sqrt(128) is
+ * orthogonal.  Accepted by dsa_indexer_qk_prepare_store and
+ * dsa_indexer_k_prepare_store; the unfused chain rejects it. */
+#define DSA_FLAG_HADAMARD 32u
 
 /*
  * Fused Q/K prepare-and-store: returns the (q_fp8, weights) contract and

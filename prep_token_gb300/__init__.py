@@ -25,6 +25,7 @@ from ._build import LIB_PATH
 __all__ = [
     "DsaError", "NEOX", "GPTJ", "HEAD_DIM", "DEVERR_POSITION", "DEVERR_SLOT", "DEVERR_TIMEOUT",
     "FLAG_PDL", "FLAG_PIPELINE", "FLAG_DIRECT", "FLAG_PDL_EARLY_ROPE", "FLAG_CACHE_TOKEN_MAJOR",
+    "FLAG_HADAMARD",
     "dsa_indexer_qk_prepare_store", "dsa_indexer_k_prepare_store", "dsa_status_string",
     "dsa_indexer_qk_prepare_store_unfused", "dsa_unfused_workspace_bytes",
     "dsa_indexer_qk_prepare_store_unfused_noalloc", "dsa_indexer_mqa_logits",
@@ -36,6 +37,7 @@ HEAD_DIM = 128
 DEVERR_POSITION, DEVERR_SLOT, DEVERR_TIMEOUT = 1, 2, 4
 FLAG_PDL, FLAG_PIPELINE, FLAG_DIRECT, FLAG_PDL_EARLY_ROPE = 1, 2, 4, 8
 FLAG_CACHE_TOKEN_MAJOR = 16
+FLAG_HADAMARD = 32
 _LAYOUT_FLAGS = {"paged": 0, "token_major": FLAG_CACHE_TOKEN_MAJOR}
 _KERNEL_FLAGS = {"auto": 0, "pipeline": FLAG_PIPELINE, "direct": FLAG_DIRECT}
 ROW_BYTES = HEAD_DIM + 4  # 128 codes + one fp32 scale per slot
@@ -228,7 +230,7 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
                                  page_size, rope_dim=64, rope_style=NEOX, *, q_fp8_out=None,
                                  weights_out=None, err_flags=None, num_tokens=None,
                                  max_position=None, pdl=False, kernel="auto",
-                                 cache_layout="paged", stream=None):
+                                 cache_layout="paged", hadamard=False, stream=None):
     """Fused Q/K prepare-and-store (one kernel launch).
 
     q [T, H, 128] bf16, k [T, 128] bf16, w [T, H] bf16 (row strides of any
@@ -245,13 +247,16 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
     choice between the two kernels (same bytes either way).
     ``cache_layout`` = "paged" (a page's codes, then its scales) or
     "token_major" (132 bytes per slot: codes, then scale).
+    ``hadamard=True`` rotates every q head and k by H_128 / sqrt(128) after
+    RoPE, before they are quantised.
     Returns (q_fp8 [T, H, 128] float8_e4m3fn, weights [T, H] fp32)."""
     args, outs, _, _ = _qk_args(q, k, w, positions, out_cache_loc, cos_cache, sin_cache,
                                 ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
                                 page_size, rope_dim, rope_style, q_fp8_out, weights_out,
                                 num_tokens, max_position)
     st = library().dsa_indexer_qk_prepare_store(
-        *args, _flags(pdl, kernel) | _layout(cache_layout), _ptr(err_flags), _stream(stream))
+        *args, _flags(pdl, kernel) | _layout(cache_layout) | (FLAG_HADAMARD if hadamard else 0),
+        _ptr(err_flags), _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store")
     return outs
@@ -323,8 +328,9 @@ def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cach
                                 ln_beta, ln_eps, index_k_cache, page_size, rope_dim=64,
                                 rope_style=NEOX, *, err_flags=None, num_tokens=None,
                                 max_position=None, pdl=False, kernel="auto",
-                                cache_layout="paged", stream=None):
-    """k-only prepare-and-store (one kernel launch); writes the cache in place."""
+                                cache_layout="paged", hadamard=False, stream=None):
+    """k-only prepare-and-store (one kernel launch); writes the cache in place.
+    ``hadamard=True`` rotates k by H_128 / sqrt(128) after RoPE."""
     cs_stride, rows = _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
                                 ln_beta, index_k_cache, rope_dim)
     T = k.shape[0] if num_tokens is None else int(num_tokens)
@@ -339,8 +345,9 @@ def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cach
         _ptr(cos_cache) if rope_dim else None, _ptr(sin_cache) if rope_dim else None,
         cs_stride, max_position, _ptr(ln_gamma), _ptr(ln_beta), float(ln_eps),
         _ptr(index_k_cache), _num_pages(index_k_cache, page_size), page_size, T, HEAD_DIM,
-        rope_dim, int(rope_style), _flags(pdl, kernel) | _layout(cache_layout), _ptr(err_flags),
-        _stream(stream))
+        rope_dim, int(rope_style),
+        _flags(pdl, kernel) | _layout(cache_layout) | (FLAG_HADAMARD if hadamard else 0),
+        _ptr(err_flags), _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_k_prepare_store")
 

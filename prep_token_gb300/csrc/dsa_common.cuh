@@ -375,14 +375,21 @@ __device__ __forceinline__ float quad_sum(float v) {
 // With A = max(amax, 1e-4) = 1.f * 2^E (normal), 448 * 2^e = 1.75 * 2^(e+8), so
 // e = E - 8 when the fraction is <= 0.75 (bits <= 0x600000) and E - 7 above:
 // read straight off the exponent and fraction bits, no division or log.
-__device__ __forceinline__ int ue8m0_exponent(const float (&x)[16]) {
+__device__ __forceinline__ float vector_amax(const float (&x)[16]) {
   float m = max3f(fabsf(x[0]), fabsf(x[1]), fabsf(x[2]));
 #pragma unroll
   for (int j = 3; j < 15; j += 2) m = max3f(m, fabsf(x[j]), fabsf(x[j + 1]));
   m = fmaxf(m, fabsf(x[15]));
-  m = fmaxf(quad_max(m), 1e-4f);
-  const uint32_t b = __float_as_uint(m);
+  return quad_max(m);
+}
+
+__device__ __forceinline__ int exponent_of_amax(float amax) {
+  const uint32_t b = __float_as_uint(fmaxf(amax, 1e-4f));
   return static_cast<int>(b >> 23) - 135 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0);
+}
+
+__device__ __forceinline__ int ue8m0_exponent(const float (&x)[16]) {
+  return exponent_of_amax(vector_amax(x));
 }
 
 // e4m3 codes of x * 2^-e (the multiply by a power of two is exact), packed in
@@ -525,6 +532,219 @@ __device__ __forceinline__ void affine_slice(const float* gamma, const float* be
   }
 }
 
+
+// ---------------------------------------------------------------- Hadamard layout
+//
+// The variant that rotates q and k by the normalised Walsh-Hadamard matrix
+// H_128 / sqrt(128) after RoPE (the rotation the fused path of sglang PR
+// "[AMD] [GLM5] Fuse the DSA indexer Q/K rope + quant + K-cache write",
+// Modifications, states it does without).  Its butterflies pair elements
+// whose indices differ in one bit, so the lane layout must make every index
+// bit either a register bit or a lane bit: each lane holds chunks of W
+// consecutive elements dealt round-robin over the 8 lanes,
+//   element (c * 8W + W * l + i)  of chunk c, offset i  ->  lane l,
+// with W = rope_dim/16 (NeoX: chunk 0 the a-members, chunk 1 the b-members),
+// 2 * rope_dim/16 (GPT-J: chunk 0 the interleaved pairs) or 16 (no RoPE).
+// The rotated chunks are exactly those of Slice, so the RoPE operands and
+// rope_slice carry over; only the pass-through elements are spread.  Index
+// bits below log2(W) and from log2(8W) up are register bits; the three in
+// between are the lane bits.  With GPT-J every chunk keeps its even elements
+// in its first W/2 registers and its odd ones in the rest (chunk 0: the a-
+// and b-members), so registers 2m and 2m+1 -- the operands of one packed
+// f32x2 instruction -- differ in the same index bit in every chunk.
+template <int STYLE, int RP>
+struct HSlice {
+  static constexpr bool NEOX = STYLE == DSA_ROPE_NEOX;
+  static constexpr bool PAIRED = !NEOX && RP > 0;  // GPT-J: chunks hold pairs
+  static constexpr int W = RP == 0 ? 16 : (NEOX ? RP : 2 * RP);
+  static constexpr int NCH = 16 / W;
+  static constexpr int STRIDE = 8 * W;  // elements from one of a lane's chunks to the next
+  // register holding element i of chunk c (x[0..RP) a-members, x[RP..2RP) b-members)
+  __host__ __device__ static constexpr int reg(int c, int i) {
+    return c * W + (PAIRED ? ((i & 1) ? W / 2 + i / 2 : i / 2) : i);
+  }
+  // element index, less the lane's W * l, of register j
+  __host__ __device__ static constexpr int off(int j) {
+    return (j / W) * STRIDE +
+           (PAIRED ? (j % W < W / 2 ? 2 * (j % W) : 2 * (j % W - W / 2) + 1) : j % W);
+  }
+  __host__ __device__ static constexpr int reg_at(int o) {
+    for (int j = 0; j < 16; ++j)
+      if (off(j) == o) return j;
+    return -1;
+  }
+  // the k-th register (in increasing order) whose element has bit B clear
+  __host__ __device__ static constexpr int low_reg(int B, int k) {
+    for (int j = 0; j < 16; ++j)
+      if ((off(j) & B) == 0 && k-- == 0) return j;
+    return -1;
+  }
+};
+
+// 2^-3.5 = 128^-0.5 rounded to fp32.
+constexpr float kHadamardScale = 0.0883883461356163f;
+
+template <int STYLE, int RP, class M>
+__device__ __forceinline__ void load_hslice(typename M::Addr row, int l, float (&x)[16]) {
+  using S = HSlice<STYLE, RP>;
+#pragma unroll
+  for (int c = 0; c < S::NCH; ++c) {
+    float t[S::W];
+    load_bf16<M, S::W, gcd_pow2(2 * S::W)>(row + 2 * (c * S::STRIDE + S::W * l), t);
+#pragma unroll
+    for (int i = 0; i < S::W; ++i) x[S::reg(c, i)] = t[i];
+  }
+}
+
+template <int STYLE, int RP>
+__device__ __forceinline__ void affine_hslice(const float* gamma, const float* beta, int l,
+                                              float (&x)[16], float rstd) {
+  using S = HSlice<STYLE, RP>;
+  constexpr int PIECE = S::W < 4 ? S::W : 4;
+#pragma unroll
+  for (int c = 0; c < S::NCH; ++c)
+#pragma unroll
+    for (int i0 = 0; i0 < S::W; i0 += PIECE) {
+      const int o = c * S::STRIDE + S::W * l + i0;
+      float g[PIECE], b[PIECE];
+      load_f32_global<PIECE, 4 * PIECE>(gamma + o, g);
+      load_f32_global<PIECE, 4 * PIECE>(beta + o, b);
+#pragma unroll
+      for (int i = 0; i < PIECE; ++i) {
+        float& v = x[S::reg(c, i0 + i)];
+        v = __fmaf_rn(__fmul_rn(v, rstd), g[i], b[i]);
+      }
+    }
+}
+
+// Butterflies on index bit log2(B) between two pairs of registers of the lane:
+// (a, b) -> (a + b, a - b), a the element with the bit clear.  Packed into
+// f32x2 instructions when both operand pairs are register pairs (2m, 2m+1).
+template <int STYLE, int RP, int B, int K>
+__device__ __forceinline__ void fwht_local_pairs(float (&x)[16]) {
+  using S = HSlice<STYLE, RP>;
+  constexpr int j0 = S::low_reg(B, K), j1 = S::low_reg(B, K + 1);
+  constexpr int p0 = S::reg_at(S::off(j0) + B), p1 = S::reg_at(S::off(j1) + B);
+  static_assert(j0 >= 0 && j1 >= 0 && p0 >= 0 && p1 >= 0, "Hadamard pair outside the lane");
+  if constexpr (j0 % 2 == 0 && j1 == j0 + 1 && p0 % 2 == 0 && p1 == p0 + 1) {
+    const float2 a = make_float2(x[j0], x[j1]);
+    const float2 b = make_float2(x[p0], x[p1]);
+    const float2 sum = __fadd2_rn(a, b);
+    const float2 dif = __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);  // a - b, one rounding
+    x[j0] = sum.x; x[j1] = sum.y;
+    x[p0] = dif.x; x[p1] = dif.y;
+  } else {
+    const float a0 = x[j0], b0 = x[p0], a1 = x[j1], b1 = x[p1];
+    x[j0] = __fadd_rn(a0, b0); x[p0] = __fsub_rn(a0, b0);
+    x[j1] = __fadd_rn(a1, b1); x[p1] = __fsub_rn(a1, b1);
+  }
+}
+
+// One butterfly stage over index bit H.  A lane bit pairs register j of lane
+// l with register j of lane l ^ m: the lane with the bit clear keeps x + y,
+// the other y - x, each one fp32 rounding of the same sum as the oracle's.
+template <int STYLE, int RP, int H>
+__device__ __forceinline__ void fwht_stage(float (&x)[16], int l) {
+  using S = HSlice<STYLE, RP>;
+  constexpr int B = 1 << H;
+  if constexpr (B >= S::W && B < S::STRIDE) {
+    constexpr int m = B / S::W;
+    const float sg = (l & m) ? -1.0f : 1.0f;
+    const float2 sg2 = make_float2(sg, sg);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const float2 y = make_float2(__shfl_xor_sync(kFull, x[j], m),
+                                   __shfl_xor_sync(kFull, x[j + 1], m));
+      const float2 r = __ffma2_rn(sg2, make_float2(x[j], x[j + 1]), y);
+      x[j] = r.x;
+      x[j + 1] = r.y;
+    }
+  } else {
+    fwht_local_pairs<STYLE, RP, B, 0>(x);
+    fwht_local_pairs<STYLE, RP, B, 2>(x);
+    fwht_local_pairs<STYLE, RP, B, 4>(x);
+    fwht_local_pairs<STYLE, RP, B, 6>(x);
+  }
+}
+
+// H_128 x (unnormalised): stages over index bits 0, 1, ..., 6 in that order.
+// The 1/sqrt(128) is applied by the quantiser.
+template <int STYLE, int RP>
+__device__ __forceinline__ void fwht_hslice(float (&x)[16], int l) {
+  fwht_stage<STYLE, RP, 0>(x, l);
+  fwht_stage<STYLE, RP, 1>(x, l);
+  fwht_stage<STYLE, RP, 2>(x, l);
+  fwht_stage<STYLE, RP, 3>(x, l);
+  fwht_stage<STYLE, RP, 4>(x, l);
+  fwht_stage<STYLE, RP, 5>(x, l);
+  fwht_stage<STYLE, RP, 6>(x, l);
+}
+
+// Scale exponent of the normalised vector y = fp32(x * 128^-0.5): rounding is
+// monotonic, so max|y| = fp32(max|x| * 128^-0.5).
+__device__ __forceinline__ int hadamard_exponent(const float (&x)[16]) {
+  return exponent_of_amax(__fmul_rn(vector_amax(x), kHadamardScale));
+}
+
+// e4m3 codes of fp32(x * 128^-0.5) * 2^-e, as fp32(x * (128^-0.5 * 2^-e)):
+// the factor is exact and scaling by a power of two commutes with rounding
+// (values small enough for that to fail give code 0 either way).  Codes
+// are packed chunk after chunk, element order inside each: byte c*W + i.
+template <int STYLE, int RP>
+__device__ __forceinline__ void quantize_hslice(const float (&x)[16], int e, uint32_t (&w)[4]) {
+  using S = HSlice<STYLE, RP>;
+  const float f = __fmul_rn(kHadamardScale, pow2f(-e));
+  const float2 f2 = make_float2(f, f);
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {  // register order: packed multiplies
+    const float2 t = __fmul2_rn(make_float2(x[j], x[j + 1]), f2);
+    v[j] = t.x;
+    v[j + 1] = t.y;
+  }
+#pragma unroll
+  for (int n = 0; n < 16; n += 2) {  // n = c * W + i: byte n of the packed codes
+    const int c0 = n / S::W, i0 = n % S::W, c1 = (n + 1) / S::W, i1 = (n + 1) % S::W;
+    const uint32_t code = cvt_e4m3x2(v[S::reg(c0, i0)], v[S::reg(c1, i1)]);
+    if ((n & 2) == 0) w[n / 4] = code;
+    else w[n / 4] |= code << 16;
+  }
+}
+
+// Store the packed codes to a 128-byte row whose start is ROW_ALIGN-aligned.
+template <int STYLE, int RP, int ROW_ALIGN = 16>
+__device__ __forceinline__ void store_hslice(uint8_t* row, int l, const uint32_t (&w)[4]) {
+  using S = HSlice<STYLE, RP>;
+  constexpr int A = gcd_pow2(S::W) < ROW_ALIGN ? gcd_pow2(S::W) : ROW_ALIGN;
+#pragma unroll
+  for (int c = 0; c < S::NCH; ++c) {
+    uint8_t* p = row + c * S::STRIDE + S::W * l;
+    if constexpr (S::W >= 4) {
+      store_codes<S::W, A>(p, w + c * S::W / 4);
+    } else {
+      const uint32_t v = w[(c * S::W) / 4] >> (8 * ((c * S::W) & 3));
+      store_codes<S::W, A>(p, &v);
+    }
+  }
+}
+
+template <int STYLE, int RP>
+__device__ __forceinline__ void store_index_k_h(const CacheGeom& g, long long slot, int l,
+                                                const uint32_t (&w)[4], int e) {
+  if (g.token_major) {
+    uint8_t* row = g.cache + slot * (kD + 4);
+    store_hslice<STYLE, RP, 4>(row, l, w);
+    if (l == 0) *reinterpret_cast<float*>(row + kD) = pow2f(e);
+  } else {
+    const long long page = slot / g.page_size;
+    const long long off = slot - page * g.page_size;
+    uint8_t* base = g.cache + page * g.page_bytes;
+    store_hslice<STYLE, RP>(base + off * kD, l, w);
+    if (l == 0)
+      *reinterpret_cast<float*>(base + static_cast<long long>(g.page_size) * kD + 4 * off) =
+          pow2f(e);
+  }
+}
 
 // bf16 of x, round to nearest even (two at a time): lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -1,0 +1,473 @@
+// DSA indexer Q/K prepare-and-store for GB300 (sm_103a): the fused kernels.
+// The launcher and the C ABI are in dsa_prep.cu; the Hadamard variant's
+// instantiations in dsa_hadamard.cu.
+//
+// The work is one streaming pass (HBM-bound, ~1 flop per byte): per token,
+// H query heads and one key of 128 bf16 each are rotated, quantised to e4m3
+// with a power-of-two scale and written out; the key is LayerNorm'd first and
+// scattered into the paged index-K cache; the gate weights absorb the query
+// scales.  (sglang PR "[AMD] [GLM5] Fuse the DSA indexer Q/K rope + quant +
+// K-cache write", Motivation and Modifications; vllm PR "[ROCm][Perf] Enable
+// fused indexer-Q RoPE+quant kernel for DeepSeek/GLM sparse attention",
+// Summary.)
+//
+// Lane layout ("balanced slices").  A quarter-warp (8 lanes) owns one
+// 128-vector; lane l holds 16 of its elements chosen so that every RoPE pair
+// sits inside one lane and every lane rotates the same number of pairs.  With
+// RP = rope_dim / 16 pairs per lane:
+//   NeoX   a-members  RP elements at  RP*l           (pair partner i + r/2)
+//          b-members  RP elements at  r/2 + RP*l
+//   GPT-J  pairs      2*RP elements at 2*RP*l        (pairs (2i, 2i+1))
+//   both   pass-through 16 - 2*RP elements at r + (16 - 2*RP)*l
+// so the lane's frequencies are RP*l .. RP*l + RP - 1 in both styles, RoPE
+// needs no shuffles, and it runs as packed f32x2 FMUL2/FFMA2.  A warp
+// handles four vectors per instruction stream.
+//
+// Two kernels share that math:
+//   * dsa_pipeline_kernel (large calls): persistent, warp-specialised.  Warp 0
+//     moves each unit -- one token and up to 64 of its heads, plus the key on
+//     the first chunk -- from HBM into a 4-stage shared-memory ring with
+//     cp.async.bulk copies counted on mbarriers; 8 consumer warps compute from
+//     shared memory and store to HBM.  Bytes in flight are set by the ring
+//     (up to ~200 KB per SM), not by registers.
+//   * dsa_direct_kernel (small calls, decode): one warp per four vectors,
+//     loads straight to registers; the least latency per call.
+// Both come in a Hadamard variant (HAD = true) that rotates every vector by
+// H_128 / sqrt(128) after RoPE; it uses the HSlice lane layout.
+// Every mbarrier wait is bounded in time (DSA_DEVERR_TIMEOUT); nothing traps.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "dsa_common.cuh"
+#include "dsa_prep.h"
+
+namespace dsa_prep_impl {
+
+using namespace dsa_dev;
+
+// ---------------------------------------------------------------- parameters
+
+struct Params {
+  const uint16_t* q;
+  long long sq_t, sq_h;
+  const uint16_t* k;
+  long long sk_t;
+  const uint16_t* w;
+  long long sw_t;
+  const long long* pos;
+  const long long* loc;
+  const float* cos_t;
+  const float* sin_t;
+  long long cs_stride;
+  long long max_pos;
+  const float* gamma;
+  const float* beta;
+  float eps;
+  float fold;  // softmax_scale * H^-0.5, rounded once to fp32
+  uint8_t* q_out;
+  float* w_out;
+  CacheGeom cg;
+  int T;
+  int H;
+  int rope_dim;
+  int cs_bytes;  // rope_dim / 2 * 4
+  // pipeline kernel
+  int HC;         // heads per unit
+  int NC;         // units per token
+  long long units;
+  int stage_bytes;
+  int w_bulk;     // the chunk's weights can be bulk-copied (16-byte aligned)
+  // direct kernel
+  int NQ;            // quads of heads per token
+  long long q_warps;  // warps doing q quads
+  long long k_warps;  // warps doing keys (four per warp)
+  int early_rope;     // read positions and cos/sin before the PDL wait
+  int* err;
+};
+
+// A bf16 row into the lane's 16 registers: the balanced slice, or the
+// Hadamard layout (HSlice) when the variant rotates by H_128.
+template <bool HAD, int STYLE, int RP, class M>
+__device__ __forceinline__ void load_vec(typename M::Addr row, int l, float (&x)[16]) {
+  if constexpr (HAD)
+    load_hslice<STYLE, RP, M>(row, l, x);
+  else
+    load_slice<STYLE, RP, M>(row, l, x);
+}
+
+// Query vector: rotate (RoPE, then H_128 / sqrt(128) in the Hadamard
+// variant), quantise, store codes; returns the scale exponent.
+template <bool HAD, int STYLE, int RP>
+__device__ __forceinline__ int q_slice(float (&x)[16], const Rot<RP>& r, uint8_t* out_row,
+                                       int l, bool store) {
+  if constexpr (RP > 0) rope_slice<RP>(x, r);
+  if constexpr (HAD) {
+    fwht_hslice<STYLE, RP>(x, l);
+    const int e = hadamard_exponent(x);
+    uint32_t w[4];
+    quantize_hslice<STYLE, RP>(x, e, w);
+    if (store) store_hslice<STYLE, RP>(out_row, l, w);
+    return e;
+  } else {
+    const int e = ue8m0_exponent(x);
+    uint32_t wa[4], wb[4], wp[4];
+    quantize_slice<STYLE, RP>(x, e, wa, wb, wp);
+    if (store) store_slice<STYLE, RP>(out_row, l, wa, wb, wp);
+    return e;
+  }
+}
+
+__device__ __forceinline__ void raise_error(const Params& p, int bit) {
+  if (p.err) atomicOr(p.err, bit);
+}
+
+// Key vector: LayerNorm (mean, biased variance, eps inside the root), RoPE
+// (then H_128 / sqrt(128) in the Hadamard variant), quantise, and store the
+// codes and the scale into slot `slot` of the cache.
+template <bool HAD, int STYLE, int RP>
+__device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const Rot<RP>& r,
+                                        int l, bool real, bool pos_ok, long long slot) {
+  float sum = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) sum = __fadd_rn(sum, x[j]);
+  const float mean = __fmul_rn(quad_sum(sum), 1.0f / kD);
+  float sq = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    x[j] = __fsub_rn(x[j], mean);
+    sq = __fmaf_rn(x[j], x[j], sq);
+  }
+  const float var = __fmul_rn(quad_sum(sq), 1.0f / kD);
+  const float rstd = __frsqrt_rn(__fadd_rn(var, p.eps));
+  if constexpr (HAD)
+    affine_hslice<STYLE, RP>(p.gamma, p.beta, l, x, rstd);
+  else
+    affine_slice<STYLE, RP>(p.gamma, p.beta, l, x, rstd);
+  if constexpr (RP > 0) rope_slice<RP>(x, r);
+  int e;
+  uint32_t wa[4], wb[4], wp[4];
+  if constexpr (HAD) {
+    fwht_hslice<STYLE, RP>(x, l);
+    e = hadamard_exponent(x);
+    quantize_hslice<STYLE, RP>(x, e, wa);
+  } else {
+    e = ue8m0_exponent(x);
+    quantize_slice<STYLE, RP>(x, e, wa, wb, wp);
+  }
+
+  if (!real) return;
+  if (!pos_ok) {
+    if (l == 0) raise_error(p, DSA_DEVERR_POSITION);
+    return;
+  }
+  if (slot < 0 || slot >= p.cg.num_slots) {
+    if (l == 0) raise_error(p, DSA_DEVERR_SLOT);
+    return;
+  }
+  if constexpr (HAD)
+    store_index_k_h<STYLE, RP>(p.cg, slot, l, wa, e);
+  else
+    store_index_k<STYLE, RP>(p.cg, slot, l, wa, wb, wp, e);
+}
+
+// ================================================================ direct kernel
+
+constexpr int kDirectThreads = 256;
+
+// cos/sin of the lane's frequencies at row `row`, from global memory.
+template <int RP>
+__device__ __forceinline__ void load_rot_global(const Params& p, long long row, int l, Rot<RP>& r) {
+  if constexpr (RP > 0) {
+    load_f32_global<RP, Slice<0, RP>::ALIGN_CS>(p.cos_t + row * p.cs_stride + RP * l, r.c);
+    load_f32_global<RP, Slice<0, RP>::ALIGN_CS>(p.sin_t + row * p.cs_stride + RP * l, r.s);
+    finish_rot<RP>(r);
+  }
+}
+
+// Position-dependent prologue of a token: its position, whether it is in
+// range, and the lane's cos/sin values.
+template <int RP>
+__device__ __forceinline__ bool token_rot(const Params& p, long long t, int l, long long& pos,
+                                          Rot<RP>& r) {
+  pos = __ldg(p.pos + t);
+  const bool pos_ok = pos >= 0 && pos < p.max_pos;
+  load_rot_global<RP>(p, pos_ok ? pos : 0, l, r);
+  return pos_ok;
+}
+
+template <bool HAD, int STYLE, int RP>
+__global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params p) {
+  const int lane = threadIdx.x & 31;
+  const int qtr = lane >> 3;
+  const int l = lane & 7;
+  const long long u = static_cast<long long>(blockIdx.x) * (kDirectThreads / 32) + (threadIdx.x >> 5);
+  const bool is_q = u < p.q_warps;
+  // q warp: four heads of one token; k warp: four keys, one per quarter-warp
+  const long long t = is_q ? u / p.NQ : 4 * (u - p.q_warps) + qtr;
+  const bool real = is_q || t < p.T;
+  const long long tt = real ? t : 0;
+  long long pos = 0;
+  bool pos_ok = false;
+  Rot<RP> r;
+  // With DSA_FLAG_PDL_EARLY_ROPE the caller guarantees that positions, slots
+  // and the cos/sin cache are not written by the previous kernel in the
+  // stream, so their two dependent round trips overlap its tail.
+  // Let the next kernel of the stream get its CTAs resident now: it waits for
+  // this grid's completion on its own griddepcontrol.wait.
+  grid_launch_dependents();
+  if (p.early_rope && u < p.q_warps + p.k_warps) pos_ok = token_rot<RP>(p, tt, l, pos, r);
+  grid_dependency_wait();
+  if (u >= p.q_warps + p.k_warps) return;  // warp-uniform
+
+  if (is_q) {
+    const int v = static_cast<int>(u - t * p.NQ) * 4 + qtr;
+    const bool valid = v < p.H;
+    // a quarter-warp past the last head re-reads head H-1 and stores nothing
+    const int vl = valid ? v : p.H - 1;
+    float x[16];
+    load_vec<HAD, STYLE, RP, GlobalMem>(
+        reinterpret_cast<const unsigned char*>(p.q + t * p.sq_t + vl * p.sq_h), l, x);
+    float wv = 0.0f;
+    if (valid && l == 0) wv = __uint_as_float(static_cast<uint32_t>(__ldg(p.w + t * p.sw_t + v)) << 16);
+    if (!p.early_rope) pos_ok = token_rot<RP>(p, t, l, pos, r);
+    const long long orow = t * p.H + v;
+    const int e = q_slice<HAD, STYLE, RP>(x, r, p.q_out + orow * kD, l, valid && pos_ok);
+    if (valid && pos_ok && l == 0) __stcs(p.w_out + orow, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold));
+  } else {
+    float x[16];
+    load_vec<HAD, STYLE, RP, GlobalMem>(reinterpret_cast<const unsigned char*>(p.k + tt * p.sk_t), l, x);
+    const long long slot = __ldg(p.loc + tt);
+    if (!p.early_rope) pos_ok = token_rot<RP>(p, tt, l, pos, r);
+    k_slice<HAD, STYLE, RP>(p, x, r, l, real, pos_ok, slot);
+  }
+}
+
+// ================================================================ pipeline kernel
+
+constexpr int kHCMax = 64;        // heads per unit at most
+constexpr int kStages = 4;        // shared-memory ring depth
+constexpr int kConsumers = 8;     // consumer warps per CTA
+constexpr int kPipeThreads = 32 * (1 + kConsumers);
+
+// stage layout (byte offsets from the stage base)
+constexpr int kOffHdr = 0;     // StageHeader
+constexpr int kOffK = 64;      // key row, 256 B
+constexpr int kOffCos = 320;   // cos row, rope_dim/2 floats (<= 256 B)
+constexpr int kOffSin = 576;   // sin row
+constexpr int kOffW = 832;     // gate weights of the chunk, HC bf16 (<= 128 B)
+constexpr int kOffQ = 1024;    // HC query rows of 256 B
+constexpr int kBarrierBytes = 128;  // full[kStages], empty[kStages], abort flag
+
+struct StageHeader {
+  long long pos;
+  long long slot;
+  int pos_ok;
+};
+
+// Producer warp: lane 0 fills the ring; all lanes prefetch (position, slot)
+// for the next 32 units of this CTA.  The position-independent copies (query
+// rows, key row, weights) go out before the position is known.
+static __device__ void producer(const Params& p, unsigned char* ring, uint32_t full0, uint32_t empty0,
+                         volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  long long my_pos = 0, my_slot = 0;
+  // (token, chunk) of unit u, advanced incrementally as u steps by gridDim.x
+  const int dt = static_cast<int>(gridDim.x) / p.NC;
+  const int dc = static_cast<int>(gridDim.x) - dt * p.NC;
+  int t = static_cast<int>(blockIdx.x) / p.NC;
+  int c = static_cast<int>(blockIdx.x) - t * p.NC;
+  int i = 0;
+  for (long long u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+    if (i > 0) {
+      t += dt;
+      c += dc;
+      if (c >= p.NC) c -= p.NC, ++t;
+    }
+    const int j = i & 31;
+    if (j == 0) {
+      const long long uu = u + static_cast<long long>(lane) * gridDim.x;
+      my_pos = 0;
+      my_slot = 0;
+      if (uu < p.units) {
+        const long long tt = uu / p.NC;
+        my_pos = __ldg(p.pos + tt);
+        if (uu - tt * p.NC == 0) my_slot = __ldg(p.loc + tt);
+      }
+    }
+    int stop = 0;
+    const int s = i % kStages;
+    const uint32_t full = full0 + 8 * s;
+    unsigned char* st = ring + static_cast<size_t>(s) * p.stage_bytes;
+    const uint32_t sts = smem_u32(st);
+    if (lane == 0) {
+      const uint32_t ph = (i / kStages) & 1;
+      if (i >= kStages && !mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag)) {
+        stop = 1;
+      } else {
+        const int h0 = c * p.HC;
+        const int n = min(p.HC, p.H - h0);
+        const uint32_t early = static_cast<uint32_t>(n) * 256u + (c == 0 ? 256u : 0u) +
+                               (p.w_bulk ? 2u * n : 0u);
+        if (early) mbar_expect_tx(full, early);
+        if (n > 0) {
+          const uint16_t* qsrc = p.q + t * p.sq_t + static_cast<long long>(h0) * p.sq_h;
+          if (p.sq_h == kD) {
+            bulk_g2s(sts + kOffQ, qsrc, static_cast<uint32_t>(n) * 256u, full);
+          } else {
+            for (int h = 0; h < n; ++h) bulk_g2s(sts + kOffQ + 256 * h, qsrc + h * p.sq_h, 256u, full);
+          }
+          if (p.w_bulk) bulk_g2s(sts + kOffW, p.w + t * p.sw_t + h0, 2u * n, full);
+        }
+        if (c == 0) bulk_g2s(sts + kOffK, p.k + t * p.sk_t, 256u, full);
+      }
+    }
+    stop = __shfl_sync(kFull, stop, 0);
+    if (stop) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        raise_error(p, DSA_DEVERR_TIMEOUT);
+      }
+      break;
+    }
+    const long long pos = __shfl_sync(kFull, my_pos, j);
+    const long long slot = __shfl_sync(kFull, my_slot, j);
+    if (lane == 0) {
+      const bool pos_ok = pos >= 0 && pos < p.max_pos;
+      const long long row = pos_ok ? pos : 0;
+      StageHeader* hd = reinterpret_cast<StageHeader*>(st + kOffHdr);
+      hd->pos = pos;
+      hd->slot = slot;
+      hd->pos_ok = pos_ok ? 1 : 0;
+      if (p.rope_dim) {
+        mbar_arrive_expect_tx(full, 2u * p.cs_bytes);
+        bulk_g2s(sts + kOffCos, p.cos_t + row * p.cs_stride, p.cs_bytes, full);
+        bulk_g2s(sts + kOffSin, p.sin_t + row * p.cs_stride, p.cs_bytes, full);
+      } else {
+        mbar_arrive(full);
+      }
+    }
+    __syncwarp();
+  }
+  // Stay until the copies of the last (up to kStages) units have landed, so
+  // the CTA never exits with a bulk copy still writing its shared memory.
+  if (lane == 0) {
+    volatile int never = 0;
+    for (int d = (i > kStages ? i - kStages : 0); d < i; ++d)
+      mbar_wait(full0 + 8 * (d % kStages), (d / kStages) & 1, &never);
+  }
+}
+
+template <bool HAD, int STYLE, int RP>
+__device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t full0,
+                         uint32_t empty0, volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  const int qtr = lane >> 3;
+  const int l = lane & 7;
+  const int dt = static_cast<int>(gridDim.x) / p.NC;
+  const int dc = static_cast<int>(gridDim.x) - dt * p.NC;
+  int t = static_cast<int>(blockIdx.x) / p.NC;
+  int c = static_cast<int>(blockIdx.x) - t * p.NC;
+  int i = 0;
+  for (long long u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+    if (i > 0) {
+      t += dt;
+      c += dc;
+      if (c >= p.NC) c -= p.NC, ++t;
+    }
+    const int s = i % kStages;
+    const uint32_t ph = (i / kStages) & 1;
+    unsigned char* st = ring + static_cast<size_t>(s) * p.stage_bytes;
+    const uint32_t sts = smem_u32(st);
+    const bool ok = mbar_wait(full0 + 8 * s, ph, abort_flag);
+    if (!__all_sync(kFull, ok)) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        raise_error(p, DSA_DEVERR_TIMEOUT);
+      }
+      return;
+    }
+    const StageHeader* hd = reinterpret_cast<const StageHeader*>(st + kOffHdr);
+    const bool pos_ok = hd->pos_ok != 0;
+    const int h0 = c * p.HC;
+    const int n = min(p.HC, p.H - h0);
+
+    Rot<RP> r;
+    if constexpr (RP > 0) {
+      load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(sts + kOffCos + 4 * RP * l, r.c);
+      load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(sts + kOffSin + 4 * RP * l, r.s);
+      finish_rot<RP>(r);
+    }
+    const long long orow0 = t * p.H + h0;
+    // query heads: warp cw takes head quads cw, cw + kConsumers, ...
+    for (int qd = cw; 4 * qd < n; qd += kConsumers) {
+      const int v = 4 * qd + qtr;
+      const bool valid = v < n;
+      // a quarter-warp past the chunk's last head re-reads it and stores nothing
+      float x[16];
+      load_vec<HAD, STYLE, RP, SharedMem>(sts + kOffQ + 256 * (valid ? v : n - 1), l, x);
+      float wv = 0.0f;
+      if (valid && l == 0)
+        wv = p.w_bulk ? __uint_as_float(static_cast<uint32_t>(
+                            *reinterpret_cast<const uint16_t*>(st + kOffW + 2 * v)) << 16)
+                      : __uint_as_float(static_cast<uint32_t>(__ldg(p.w + t * p.sw_t + h0 + v)) << 16);
+      const int e = q_slice<HAD, STYLE, RP>(x, r, p.q_out + (orow0 + v) * kD, l, valid && pos_ok);
+      if (valid && pos_ok && l == 0)
+        __stcs(p.w_out + orow0 + v, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold));
+    }
+    // the key rides with chunk 0; the warp that takes it rotates per unit
+    if (c == 0 && cw == i % kConsumers) {
+      float x[16];
+      load_vec<HAD, STYLE, RP, SharedMem>(sts + kOffK, l, x);
+      k_slice<HAD, STYLE, RP>(p, x, r, l, qtr == 0, pos_ok, hd->slot);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+  }
+}
+
+template <bool HAD, int STYLE, int RP>
+__global__ void __launch_bounds__(kPipeThreads, 3) dsa_pipeline_kernel(const Params p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
+  unsigned char* ring = smem + kBarrierBytes;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kConsumers);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // inputs may be written by the kernel before this one in the stream (PDL)
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  const int warp = threadIdx.x >> 5;
+  if (warp == 0)
+    producer(p, ring, full0, empty0, abort_flag);
+  else
+    consumer<HAD, STYLE, RP>(p, warp - 1, ring, full0, empty0, abort_flag);
+}
+
+// ---------------------------------------------------------------- kernel tables
+
+using KernelFn = void (*)(Params);
+
+template <bool HAD, int STYLE, int RP>
+constexpr KernelFn pipeline_fn() { return dsa_pipeline_kernel<HAD, STYLE, RP>; }
+template <bool HAD, int STYLE, int RP>
+constexpr KernelFn direct_fn() { return dsa_direct_kernel<HAD, STYLE, RP>; }
+
+// The Hadamard variant's kernels, [rope_style][rope_dim / 16 -> 0, 1, 2, 4, 8];
+// instantiated in their own translation unit.
+extern const KernelFn kPipelineHad[2][5];
+extern const KernelFn kDirectHad[2][5];
+
+}  // namespace dsa_prep_impl

@@ -336,3 +336,24 @@ def test_hadamard_variant_bruteforce_tiny(style):
         kc, ke = quant64(Hm @ rope64(y, inp.cos[p], inp.sin[p], 64, style))
         assert ke == out["k_exp"][t]
         assert code_distance(codes[inp.slots[t]], kc).max() <= 1
+
+
+def test_worked_hadamard(worked):
+    ex, kx = worked["hadamard"], worked["k_identity"]
+    q = synth.to_bf16_bits(np.array(_expand(ex["q"]), np.float32))
+    k = synth.to_bf16_bits(np.array(_expand(kx["k"]), np.float32))
+    w = synth.to_bf16_bits(np.array([ex["w"]], np.float32))
+    cache = np.full(64 * 132, SENTINEL, np.uint8)
+    q_fp8 = np.zeros((1, 1, 128), np.uint8)
+    weights = np.zeros((1, 1), np.float32)
+    err, qe, ke = oracle.qk_prepare_store(
+        q, 128, 128, k, 128, w, 1, np.array([0], np.int64), np.array([0], np.int64),
+        np.ones((1, 32), np.float32), np.zeros((1, 32), np.float32), 32, 1,
+        np.ones(128, np.float32), np.zeros(128, np.float32), kx["eps"], ex["softmax_scale"],
+        q_fp8, weights, cache, 1, 64, 1, 64, oracle.NEOX, hadamard=True)
+    assert err == 0
+    assert qe[0, 0] == ex["expect_q_exp"] and ke[0] == ex["expect_k_exp"]
+    assert list(q_fp8[0, 0]) == _expand(ex["expect_q_codes"])
+    assert weights[0, 0] == np.float32(ex["expect_weight"])
+    assert list(cache[:128]) == _expand(ex["expect_k_codes"])
+    assert cache[64 * 128:64 * 128 + 4].view(np.float32)[0] == np.float32(2.0 ** -5)
