@@ -224,47 +224,57 @@ __device__ __forceinline__ void load_f32_shared(uint32_t a, float* x) {
   for (int j = 0; j < N; ++j) x[j] = __uint_as_float(w[j]);
 }
 
-// Store `BYTES` code bytes (packed little-endian in w[]) at global p.
-// Store `BYTES` bytes (packed little-endian in w[]) at global p.  STREAM
-// selects the evict-first cache hint for data this pass will not read again.
+// Store `BYTES` bytes (packed little-endian in w[]) at global p when `pred`
+// holds.  The predicate goes on the store instructions themselves, so a
+// quarter-warp that skips its store costs no branch.  STREAM selects the
+// evict-first cache hint for data this pass will not read again.
+#define DSA_ST_PRED(OP, ...)                                                            \
+  asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n @q " OP "\n}" ::__VA_ARGS__ \
+               : "memory")
 template <int BYTES, int ALIGN, bool STREAM = true>
-__device__ __forceinline__ void store_codes(uint8_t* p, const uint32_t* w) {
+__device__ __forceinline__ void store_codes(uint8_t* p, const uint32_t* w, bool pred = true) {
   constexpr int W = pow2_floor(ALIGN < BYTES ? ALIGN : BYTES);
+  const uint32_t q = pred ? 1u : 0u;
 #pragma unroll
   for (int b = 0; b < BYTES; b += W) {
     if constexpr (W == 16) {
       if constexpr (STREAM)
-        asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p + b), "r"(w[b / 4]),
-                     "r"(w[b / 4 + 1]), "r"(w[b / 4 + 2]), "r"(w[b / 4 + 3]) : "memory");
+        DSA_ST_PRED("st.global.cs.v4.u32 [%1], {%2,%3,%4,%5};", "r"(q), "l"(p + b), "r"(w[b / 4]),
+                    "r"(w[b / 4 + 1]), "r"(w[b / 4 + 2]), "r"(w[b / 4 + 3]));
       else
-        asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p + b), "r"(w[b / 4]),
-                     "r"(w[b / 4 + 1]), "r"(w[b / 4 + 2]), "r"(w[b / 4 + 3]) : "memory");
+        DSA_ST_PRED("st.global.v4.u32 [%1], {%2,%3,%4,%5};", "r"(q), "l"(p + b), "r"(w[b / 4]),
+                    "r"(w[b / 4 + 1]), "r"(w[b / 4 + 2]), "r"(w[b / 4 + 3]));
     } else if constexpr (W == 8) {
       if constexpr (STREAM)
-        asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p + b), "r"(w[b / 4]),
-                     "r"(w[b / 4 + 1]) : "memory");
+        DSA_ST_PRED("st.global.cs.v2.u32 [%1], {%2,%3};", "r"(q), "l"(p + b), "r"(w[b / 4]),
+                    "r"(w[b / 4 + 1]));
       else
-        asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p + b), "r"(w[b / 4]),
-                     "r"(w[b / 4 + 1]) : "memory");
+        DSA_ST_PRED("st.global.v2.u32 [%1], {%2,%3};", "r"(q), "l"(p + b), "r"(w[b / 4]),
+                    "r"(w[b / 4 + 1]));
     } else if constexpr (W == 4) {
       if constexpr (STREAM)
-        asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p + b), "r"(w[b / 4]) : "memory");
+        DSA_ST_PRED("st.global.cs.u32 [%1], %2;", "r"(q), "l"(p + b), "r"(w[b / 4]));
       else
-        asm volatile("st.global.u32 [%0], %1;" ::"l"(p + b), "r"(w[b / 4]) : "memory");
+        DSA_ST_PRED("st.global.u32 [%1], %2;", "r"(q), "l"(p + b), "r"(w[b / 4]));
     } else if constexpr (W == 2) {
       const uint16_t v = static_cast<uint16_t>(w[b / 4] >> (8 * (b & 3)));
       if constexpr (STREAM)
-        asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p + b), "h"(v) : "memory");
+        DSA_ST_PRED("st.global.cs.u16 [%1], %2;", "r"(q), "l"(p + b), "h"(v));
       else
-        asm volatile("st.global.u16 [%0], %1;" ::"l"(p + b), "h"(v) : "memory");
+        DSA_ST_PRED("st.global.u16 [%1], %2;", "r"(q), "l"(p + b), "h"(v));
     } else {
       const uint16_t v = static_cast<uint16_t>((w[b / 4] >> (8 * (b & 3))) & 0xff);
       if constexpr (STREAM)
-        asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p + b), "h"(v) : "memory");
+        DSA_ST_PRED("st.global.cs.u8 [%1], %2;", "r"(q), "l"(p + b), "h"(v));
       else
-        asm volatile("st.global.u8 [%0], %1;" ::"l"(p + b), "h"(v) : "memory");
+        DSA_ST_PRED("st.global.u8 [%1], %2;", "r"(q), "l"(p + b), "h"(v));
     }
   }
+}
+
+// One fp32 at global p when `pred` holds (evict-first), without a branch.
+__device__ __forceinline__ void store_f32_cs(float* p, float v, bool pred) {
+  DSA_ST_PRED("st.global.cs.f32 [%1], %2;", "r"(pred ? 1u : 0u), "l"(p), "f"(v));
 }
 
 // ---------------------------------------------------------------- the slice
@@ -439,20 +449,21 @@ __device__ __forceinline__ void quantize_slice(const float (&x)[16], int e, uint
 // Store the lane's codes to a 128-byte row whose start is ROW_ALIGN-aligned.
 template <int STYLE, int RP, int ROW_ALIGN = 16>
 __device__ __forceinline__ void store_slice(uint8_t* row, int l, const uint32_t* wa,
-                                            const uint32_t* wb, const uint32_t* wp) {
+                                            const uint32_t* wb, const uint32_t* wp,
+                                            bool pred = true) {
   using S = Slice<STYLE, RP>;
   constexpr int AA = S::ALIGN_A_U8 < ROW_ALIGN ? S::ALIGN_A_U8 : ROW_ALIGN;
   constexpr int AB = S::ALIGN_B_U8 < ROW_ALIGN ? S::ALIGN_B_U8 : ROW_ALIGN;
   constexpr int AP = S::ALIGN_P_U8 < ROW_ALIGN ? S::ALIGN_P_U8 : ROW_ALIGN;
   if constexpr (RP > 0) {
     if constexpr (S::NEOX) {
-      store_codes<RP, AA>(row + RP * l, wa);
-      store_codes<RP, AB>(row + S::B_BASE + RP * l, wb);
+      store_codes<RP, AA>(row + RP * l, wa, pred);
+      store_codes<RP, AB>(row + S::B_BASE + RP * l, wb, pred);
     } else {
-      store_codes<2 * RP, AA>(row + 2 * RP * l, wa);
+      store_codes<2 * RP, AA>(row + 2 * RP * l, wa, pred);
     }
   }
-  if constexpr (S::NP > 0) store_codes<S::NP, AP>(row + S::P_BASE + S::NP * l, wp);
+  if constexpr (S::NP > 0) store_codes<S::NP, AP>(row + S::P_BASE + S::NP * l, wp, pred);
 }
 
 // Index-K cache geometry and the store of one key's codes and scale into it.
@@ -713,17 +724,18 @@ __device__ __forceinline__ void quantize_hslice(const float (&x)[16], int e, uin
 
 // Store the packed codes to a 128-byte row whose start is ROW_ALIGN-aligned.
 template <int STYLE, int RP, int ROW_ALIGN = 16>
-__device__ __forceinline__ void store_hslice(uint8_t* row, int l, const uint32_t (&w)[4]) {
+__device__ __forceinline__ void store_hslice(uint8_t* row, int l, const uint32_t (&w)[4],
+                                             bool pred = true) {
   using S = HSlice<STYLE, RP>;
   constexpr int A = gcd_pow2(S::W) < ROW_ALIGN ? gcd_pow2(S::W) : ROW_ALIGN;
 #pragma unroll
   for (int c = 0; c < S::NCH; ++c) {
     uint8_t* p = row + c * S::STRIDE + S::W * l;
     if constexpr (S::W >= 4) {
-      store_codes<S::W, A>(p, w + c * S::W / 4);
+      store_codes<S::W, A>(p, w + c * S::W / 4, pred);
     } else {
       const uint32_t v = w[(c * S::W) / 4] >> (8 * ((c * S::W) & 3));
-      store_codes<S::W, A>(p, &v);
+      store_codes<S::W, A>(p, &v, pred);
     }
   }
 }

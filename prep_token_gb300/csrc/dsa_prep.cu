@@ -137,7 +137,8 @@ cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligne
         &cfg, (flags & DSA_FLAG_HADAMARD) ? kDirectHad[rope_style][ri] : kDirect[rope_style][ri], p);
   }
   choose_units(p, sms, w_rows_aligned);
-  const int per_sm = p.HC >= 32 ? 3 : 6;
+  // one wave of persistent CTAs: as many as are resident at once
+  const int per_sm = (flags & DSA_FLAG_HADAMARD) ? kPipeCtasHad : kPipeCtas;
   long long blocks = static_cast<long long>(sms) * per_sm;
   if (blocks > p.units) blocks = p.units;
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));

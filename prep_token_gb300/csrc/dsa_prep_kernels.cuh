@@ -109,13 +109,13 @@ __device__ __forceinline__ int q_slice(float (&x)[16], const Rot<RP>& r, uint8_t
     const int e = hadamard_exponent(x);
     uint32_t w[4];
     quantize_hslice<STYLE, RP>(x, e, w);
-    if (store) store_hslice<STYLE, RP>(out_row, l, w);
+    store_hslice<STYLE, RP>(out_row, l, w, store);
     return e;
   } else {
     const int e = ue8m0_exponent(x);
     uint32_t wa[4], wb[4], wp[4];
     quantize_slice<STYLE, RP>(x, e, wa, wb, wp);
-    if (store) store_slice<STYLE, RP>(out_row, l, wa, wb, wp);
+    store_slice<STYLE, RP>(out_row, l, wa, wb, wp, store);
     return e;
   }
 }
@@ -230,12 +230,12 @@ __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params
     float x[16];
     load_vec<HAD, STYLE, RP, GlobalMem>(
         reinterpret_cast<const unsigned char*>(p.q + t * p.sq_t + vl * p.sq_h), l, x);
-    float wv = 0.0f;
-    if (valid && l == 0) wv = __uint_as_float(static_cast<uint32_t>(__ldg(p.w + t * p.sw_t + v)) << 16);
+    const float wv = __uint_as_float(static_cast<uint32_t>(__ldg(p.w + t * p.sw_t + vl)) << 16);
     if (!p.early_rope) pos_ok = token_rot<RP>(p, t, l, pos, r);
     const long long orow = t * p.H + v;
     const int e = q_slice<HAD, STYLE, RP>(x, r, p.q_out + orow * kD, l, valid && pos_ok);
-    if (valid && pos_ok && l == 0) __stcs(p.w_out + orow, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold));
+    store_f32_cs(p.w_out + orow, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold),
+                 valid && pos_ok && l == 0);
   } else {
     float x[16];
     load_vec<HAD, STYLE, RP, GlobalMem>(reinterpret_cast<const unsigned char*>(p.k + tt * p.sk_t), l, x);
@@ -251,6 +251,10 @@ constexpr int kHCMax = 64;        // heads per unit at most
 constexpr int kStages = 4;        // shared-memory ring depth
 constexpr int kConsumers = 8;     // consumer warps per CTA
 constexpr int kPipeThreads = 32 * (1 + kConsumers);
+// Resident CTAs per SM the pipeline kernels are compiled for (registers per
+// thread <= 65536 / (kPipeThreads * this)); the launcher sizes grids to match.
+constexpr int kPipeCtas = 3;
+constexpr int kPipeCtasHad = 3;
 
 // stage layout (byte offsets from the stage base)
 constexpr int kOffHdr = 0;     // StageHeader
@@ -401,21 +405,24 @@ __device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t 
       finish_rot<RP>(r);
     }
     const long long orow0 = t * p.H + h0;
+    // One query head of the chunk for this quarter-warp: head v (a quarter-
+    // warp past the chunk's last head re-reads it and stores nothing).
+    auto q_head = [&](int v, float (&x)[16]) {
+      const bool valid = v < n;
+      const int vl = valid ? v : n - 1;
+      load_vec<HAD, STYLE, RP, SharedMem>(sts + kOffQ + 256 * vl, l, x);
+      const float wv =
+          p.w_bulk ? __uint_as_float(static_cast<uint32_t>(
+                         *reinterpret_cast<const uint16_t*>(st + kOffW + 2 * vl)) << 16)
+                   : __uint_as_float(static_cast<uint32_t>(__ldg(p.w + t * p.sw_t + h0 + vl)) << 16);
+      const int e = q_slice<HAD, STYLE, RP>(x, r, p.q_out + (orow0 + v) * kD, l, valid && pos_ok);
+      store_f32_cs(p.w_out + orow0 + v, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold),
+                   valid && pos_ok && l == 0);
+    };
     // query heads: warp cw takes head quads cw, cw + kConsumers, ...
     for (int qd = cw; 4 * qd < n; qd += kConsumers) {
-      const int v = 4 * qd + qtr;
-      const bool valid = v < n;
-      // a quarter-warp past the chunk's last head re-reads it and stores nothing
       float x[16];
-      load_vec<HAD, STYLE, RP, SharedMem>(sts + kOffQ + 256 * (valid ? v : n - 1), l, x);
-      float wv = 0.0f;
-      if (valid && l == 0)
-        wv = p.w_bulk ? __uint_as_float(static_cast<uint32_t>(
-                            *reinterpret_cast<const uint16_t*>(st + kOffW + 2 * v)) << 16)
-                      : __uint_as_float(static_cast<uint32_t>(__ldg(p.w + t * p.sw_t + h0 + v)) << 16);
-      const int e = q_slice<HAD, STYLE, RP>(x, r, p.q_out + (orow0 + v) * kD, l, valid && pos_ok);
-      if (valid && pos_ok && l == 0)
-        __stcs(p.w_out + orow0 + v, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold));
+      q_head(4 * qd + qtr, x);
     }
     // the key rides with chunk 0; the warp that takes it rotates per unit
     if (c == 0 && cw == i % kConsumers) {
@@ -429,7 +436,8 @@ __device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t 
 }
 
 template <bool HAD, int STYLE, int RP>
-__global__ void __launch_bounds__(kPipeThreads, 3) dsa_pipeline_kernel(const Params p) {
+__global__ void __launch_bounds__(kPipeThreads, HAD ? kPipeCtasHad : kPipeCtas)
+    dsa_pipeline_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
