@@ -11,7 +11,10 @@ kernel launch.  Prints ONE JSON line (rank 0):
              from the 129 MB L2)
   e2e        the same through the public Python API with pinned host buffers:
              host->device copy of q, k|w, positions and slots, the call, and
-             device->host copy of (q_fp8, weights), all inside the timed region
+             device->host copy of (q_fp8, weights), all inside the timed region;
+             steps alternate between two streams so one step's device->host
+             copy overlaps the next one's host->device copy (the one-stream
+             figure is reported beside it)
   roofline   algorithmic bytes per launch / launch time vs the measured HBM
              copy bandwidth; traffic = DRAM bytes per launch from the committed
              ncu summary when it was taken on the current kernel source
@@ -385,41 +388,55 @@ def run_ours(args, rank, world, local_rank):
     launch_us = ms_per_step * 1000.0
     achieved = algo_bytes / (launch_us * 1e-6) / 1e9
 
-    # end to end through the public API, host buffers, copies inside the region
-    inp0, d0 = sets[0]
+    # end to end through the public API, host buffers, copies inside the region.
+    # Steps alternate between two streams, each with its own device buffers
+    # and pinned host outputs, so one step's device->host copy overlaps the
+    # next step's host->device copy (the two directions of the host link).
+    inp0 = sets[0][0]
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
     h_q = pin(inp0.q.view(np.int16)).view(torch.bfloat16)
     h_kw = pin(inp0.kw.view(np.int16)).view(torch.bfloat16)
     h_pos, h_slots = pin(inp0.positions), pin(inp0.slots)
-    h_qo = torch.empty((T, H, 128), dtype=torch.uint8).pin_memory()
-    h_wo = torch.empty((T, H), dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, min(50, args.steps))
+    h_out = [(torch.empty((T, H, 128), dtype=torch.uint8).pin_memory(),
+              torch.empty((T, H), dtype=torch.float32).pin_memory()) for _ in range(2)]
+    lanes = [(torch.cuda.Stream(device=dev), sets[j][1], h_out[j]) for j in range(2)]
+    e2e_steps = max(4, min(50, args.steps))
 
-    def e2e_step():
-        d0["q"].copy_(h_q, non_blocking=True)
-        d0["kw"].copy_(h_kw, non_blocking=True)
-        d0["positions"].copy_(h_pos, non_blocking=True)
-        d0["slots"].copy_(h_slots, non_blocking=True)
-        _call(dp, inp0, d0, stream)
-        h_qo.copy_(d0["q_out"].view(torch.uint8), non_blocking=True)
-        h_wo.copy_(d0["w_out"], non_blocking=True)
+    def e2e_step(i, lane=None):
+        s, d, (h_qo, h_wo) = lanes[i & 1] if lane is None else lanes[lane]
+        with torch.cuda.stream(s):
+            d["q"].copy_(h_q, non_blocking=True)
+            d["kw"].copy_(h_kw, non_blocking=True)
+            d["positions"].copy_(h_pos, non_blocking=True)
+            d["slots"].copy_(h_slots, non_blocking=True)
+            _call(dp, inp0, d, s)
+            h_qo.copy_(d["q_out"].view(torch.uint8), non_blocking=True)
+            h_wo.copy_(d["w_out"], non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
-        stream.synchronize()
+    def e2e_region(serial):
+        for i in range(2):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
         if world > 1:
             torch.distributed.barrier()
+        s0 = lanes[0][0]
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        f1.record(stream)
-    stream.synchronize()
-    e2e_ms = max_over_ranks(f0.elapsed_time(f1), dev)
+        f0.record(s0)
+        lanes[1][0].wait_event(f0)
+        for i in range(e2e_steps):
+            e2e_step(i, 0 if serial else None)
+        done = torch.cuda.Event()
+        done.record(lanes[1][0])
+        s0.wait_event(done)
+        f1.record(s0)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(f0.elapsed_time(f1), dev)
+
+    e2e_serial_ms = e2e_region(serial=True)
+    e2e_ms = e2e_region(serial=False)
     h2d = h_q.numel() * 2 + h_kw.numel() * 2 + h_pos.numel() * 8 + h_slots.numel() * 8
-    d2h = h_qo.numel() + h_wo.numel() * 4
+    d2h = h_out[0][0].numel() + h_out[0][1].numel() * 4
 
     # the unfused four-launch chain on the same prefill inputs (baseline)
     unfused = None
@@ -499,7 +516,9 @@ def run_ours(args, rank, world, local_rank):
                      "nominal_frac_8tbs": achieved / 8000.0},
         "e2e": {"value": world * T * e2e_steps / (e2e_ms / 1000.0), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms / e2e_steps},
+                "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
+                "streams": 2, "serial_ms_per_step": e2e_serial_ms / e2e_steps,
+                "host_link_gb_per_s": (h2d + d2h) / (e2e_ms / e2e_steps) / 1e6},
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
         "decode": decode,

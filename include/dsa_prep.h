@@ -131,6 +131,15 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
  * orthogonal.  Accepted by dsa_indexer_qk_prepare_store and
  * dsa_indexer_k_prepare_store; the unfused chain rejects it. */
 #define DSA_FLAG_HADAMARD 32u
+/* TEST ONLY, with DSA_FLAG_PIPELINE: the producer warp of the pipeline
+ * kernel's first CTA withholds the copies of its first unit and never marks
+ * that stage full.  That CTA's consumers then give up their bounded waits
+ * (2 s each), the CTA stops, and the call sets DSA_DEVERR_TIMEOUT in
+ * *err_flags; the outputs of that CTA's units are unspecified and every other
+ * CTA completes normally.  It exists so the timeout path can be tested
+ * without a fault; the context stays usable.  Without DSA_FLAG_PIPELINE this
+ * flag is an error. */
+#define DSA_FLAG_TEST_WITHHOLD_UNIT (1u << 30)
 
 /*
  * Fused Q/K prepare-and-store: returns the (q_fp8, weights) contract and

@@ -38,6 +38,7 @@ DEVERR_POSITION, DEVERR_SLOT, DEVERR_TIMEOUT = 1, 2, 4
 FLAG_PDL, FLAG_PIPELINE, FLAG_DIRECT, FLAG_PDL_EARLY_ROPE = 1, 2, 4, 8
 FLAG_CACHE_TOKEN_MAJOR = 16
 FLAG_HADAMARD = 32
+FLAG_TEST_WITHHOLD_UNIT = 1 << 30  # test only: see include/dsa_prep.h
 _LAYOUT_FLAGS = {"paged": 0, "token_major": FLAG_CACHE_TOKEN_MAJOR}
 _KERNEL_FLAGS = {"auto": 0, "pipeline": FLAG_PIPELINE, "direct": FLAG_DIRECT}
 ROW_BYTES = HEAD_DIM + 4  # 128 codes + one fp32 scale per slot

@@ -120,6 +120,7 @@ cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligne
     cfg.numAttrs = 1;
   }
   p.early_rope = (flags & DSA_FLAG_PDL_EARLY_ROPE) ? 1 : 0;
+  p.test_withhold = (flags & DSA_FLAG_TEST_WITHHOLD_UNIT) ? 1 : 0;
   p.cg.token_major = (flags & DSA_FLAG_CACHE_TOKEN_MAJOR) ? 1 : 0;
   const long long vecs = static_cast<long long>(p.T) * (p.H > 0 ? p.H : 1);
   bool direct = vecs <= kDirectMaxVectors;
@@ -161,7 +162,9 @@ dsa_status check_k_side(const void* k, int64_t k_stride_t, const int64_t* positi
   if (rope_style != DSA_ROPE_NEOX && rope_style != DSA_ROPE_GPTJ) return DSA_ERR_UNSUPPORTED;
   if (flags & ~static_cast<uint32_t>(DSA_FLAG_PDL | DSA_FLAG_PIPELINE | DSA_FLAG_DIRECT |
                                      DSA_FLAG_PDL_EARLY_ROPE | DSA_FLAG_CACHE_TOKEN_MAJOR |
-                                     DSA_FLAG_HADAMARD))
+                                     DSA_FLAG_HADAMARD | DSA_FLAG_TEST_WITHHOLD_UNIT))
+    return DSA_ERR_UNSUPPORTED;
+  if ((flags & DSA_FLAG_TEST_WITHHOLD_UNIT) && !(flags & DSA_FLAG_PIPELINE))
     return DSA_ERR_UNSUPPORTED;
   if ((flags & DSA_FLAG_PDL_EARLY_ROPE) && !(flags & DSA_FLAG_PDL)) return DSA_ERR_UNSUPPORTED;
   if ((flags & DSA_FLAG_PIPELINE) && (flags & DSA_FLAG_DIRECT)) return DSA_ERR_UNSUPPORTED;

@@ -85,6 +85,7 @@ struct Params {
   long long q_warps;  // warps doing q quads
   long long k_warps;  // warps doing keys (four per warp)
   int early_rope;     // read positions and cos/sin before the PDL wait
+  int test_withhold;  // DSA_FLAG_TEST_WITHHOLD_UNIT
   int* err;
 };
 
@@ -306,11 +307,13 @@ static __device__ void producer(const Params& p, unsigned char* ring, uint32_t f
     const uint32_t full = full0 + 8 * s;
     unsigned char* st = ring + static_cast<size_t>(s) * p.stage_bytes;
     const uint32_t sts = smem_u32(st);
+    // test hook: CTA 0 never fills its first stage (see DSA_FLAG_TEST_WITHHOLD_UNIT)
+    const bool withhold = p.test_withhold && blockIdx.x == 0 && i == 0;
     if (lane == 0) {
       const uint32_t ph = (i / kStages) & 1;
       if (i >= kStages && !mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag)) {
         stop = 1;
-      } else {
+      } else if (!withhold) {
         const int h0 = c * p.HC;
         const int n = min(p.HC, p.H - h0);
         const uint32_t early = static_cast<uint32_t>(n) * 256u + (c == 0 ? 256u : 0u) +
@@ -338,7 +341,7 @@ static __device__ void producer(const Params& p, unsigned char* ring, uint32_t f
     }
     const long long pos = __shfl_sync(kFull, my_pos, j);
     const long long slot = __shfl_sync(kFull, my_slot, j);
-    if (lane == 0) {
+    if (lane == 0 && !withhold) {
       const bool pos_ok = pos >= 0 && pos < p.max_pos;
       const long long row = pos_ok ? pos : 0;
       StageHeader* hd = reinterpret_cast<StageHeader*>(st + kOffHdr);

@@ -70,6 +70,7 @@ def _k(lib, **over):
     (dict(g=A + 4), 2), (dict(cache=A + 8), 2), (dict(cos=A + 4), 2), (dict(cs=34), 2),
     (dict(cs=16), 3), (dict(skt=-128), 3), (dict(flags=64), 4), (dict(flags=6), 4), (dict(flags=8), 4),
     (dict(flags=32 | 8), 4), (dict(flags=32 | 6), 4), (dict(flags=0x80000000), 4),
+    (dict(flags=1 << 30), 4), (dict(flags=(1 << 30) | 4), 4),
     (dict(r=48), 4), (dict(r=96), 4), (dict(r=112), 4),
 ])
 def test_k_side_validation(lib, over, status):
