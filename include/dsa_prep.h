@@ -91,6 +91,9 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
 #define DSA_DEVERR_POSITION 1 /* a position outside [0, max_position) */
 #define DSA_DEVERR_SLOT 2     /* a slot outside [0, num_pages * page_size) */
 #define DSA_DEVERR_TIMEOUT 4  /* an internal wait gave up (never expected) */
+#define DSA_DEVERR_INTERNAL 8 /* an internal precondition failed: the logits
+                                 kernel's shared-memory base was not 1024-byte
+                                 aligned (never expected); nothing was written */
 
 /* Launch flags. */
 #define DSA_FLAG_PDL 1u /* programmatic dependent launch: the kernel may start

@@ -24,6 +24,7 @@ from ._build import LIB_PATH
 
 __all__ = [
     "DsaError", "NEOX", "GPTJ", "HEAD_DIM", "DEVERR_POSITION", "DEVERR_SLOT", "DEVERR_TIMEOUT",
+    "DEVERR_INTERNAL",
     "FLAG_PDL", "FLAG_PIPELINE", "FLAG_DIRECT", "FLAG_PDL_EARLY_ROPE", "FLAG_CACHE_TOKEN_MAJOR",
     "FLAG_HADAMARD",
     "dsa_indexer_qk_prepare_store", "dsa_indexer_k_prepare_store", "dsa_status_string",
@@ -34,7 +35,7 @@ __all__ = [
 
 NEOX, GPTJ = 0, 1
 HEAD_DIM = 128
-DEVERR_POSITION, DEVERR_SLOT, DEVERR_TIMEOUT = 1, 2, 4
+DEVERR_POSITION, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1, 2, 4, 8
 FLAG_PDL, FLAG_PIPELINE, FLAG_DIRECT, FLAG_PDL_EARLY_ROPE = 1, 2, 4, 8
 FLAG_CACHE_TOKEN_MAJOR = 16
 FLAG_HADAMARD = 32

@@ -84,6 +84,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+// Hint: bring `bytes` (a multiple of 16, 16-byte aligned) at global p into L2.
+// L2 is the GPU's point of coherence, so a line prefetched before another
+// kernel writes it is updated by that write; nothing is cached nearer.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Programmatic dependent launch: no-ops unless the launch carries the attribute.
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");

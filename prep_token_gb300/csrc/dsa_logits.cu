@@ -10,13 +10,15 @@
 // One CTA works on one query token t and a strided set of 128-key tiles
 // (two 64-key pages each).  Per tile:
 //   * warp 0 (one lane) issues two 3-D TMA loads (128B swizzle) of the pages'
-//     code blocks straight from the paged cache into a 4-stage ring;
+//     code blocks straight from the paged cache into a 4-stage ring, and a
+//     bulk copy of each page's 256-byte scale block beside them;
 //   * warp 1 (one lane) issues four tcgen05.mma.kind::f8f6f4 (M = 128 keys,
 //     N = H heads, K = 32 each) into one of two TMEM accumulators, and commits
 //     them to the "stage free" and "accumulator full" mbarriers;
 //   * warps 2..5 read their 32 TMEM lanes (one key per thread, H fp32 per key)
 //     with tcgen05.ld, release the accumulator, and reduce over heads with
-//     ReLU and the gate weights, times the key's scale.
+//     ReLU and the gate weights, times the key's scale (from shared memory;
+//     the stage is refilled only after all four warps have read it).
 // Every wait is bounded in time; TMEM is always released before exit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -140,7 +142,8 @@ struct LSmem {
   static constexpr int kQBytes = NH * kD;                       // B operand
   static constexpr int kOffQ = 0;                               // 1024-aligned
   static constexpr int kOffK = ((kQBytes + 1023) / 1024) * 1024;  // A stages
-  static constexpr int kOffW = kOffK + kKStages * kTileBytes;    // weights[NH]
+  static constexpr int kOffS = kOffK + kKStages * kTileBytes;    // key scales, 128 per stage
+  static constexpr int kOffW = kOffS + kKStages * kTileKeys * 4;  // weights[NH]
   static constexpr int kOffBar = kOffW + NH * 4;
   // barriers: full[S], empty[S], qfull, accfull[2], accempty[2], drain
   static constexpr int kBars = 2 * kKStages + 6;
@@ -155,11 +158,15 @@ __global__ void __launch_bounds__(kLThreads, 1)
     dsa_mqa_logits_kernel(const __grid_constant__ CUtensorMap tq,
                           const __grid_constant__ CUtensorMap tk, const LParams p) {
   using L = LSmem<NH>;
-  extern __shared__ unsigned char smem_raw[];
-  // 1024-byte alignment for the 128-byte-swizzled tiles
-  const uint32_t raw = smem_u32(smem_raw);
-  unsigned char* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  extern __shared__ __align__(1024) unsigned char smem[];
+  // The 128-byte-swizzled tiles need a 1024-byte aligned base.  The dynamic
+  // shared window of a kernel without static shared memory starts on such a
+  // boundary; should it ever not, report it and leave before taking anything.
   const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0 && p.err) atomicOr(p.err, DSA_DEVERR_INTERNAL);
+    return;
+  }
   const uint32_t bar0 = sbase + L::kOffBar;
   auto full = [&](int s) { return bar0 + 8 * s; };
   auto empty = [&](int s) { return bar0 + 8 * (kKStages + s); };
@@ -177,7 +184,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 1);
+      mbar_init(empty(s), 1 + 4);  // the MMA commit and the four epilogue warps
     }
     mbar_init(qfull, 1);
     for (int b = 0; b < 2; ++b) {
@@ -221,14 +228,16 @@ __global__ void __launch_bounds__(kLThreads, 1)
         }
         const int blk0 = 2 * i, blk1 = 2 * i + 1;
         const bool has1 = blk1 * kPageKeys < len;
-        mbar_arrive_expect_tx(full(s), has1 ? kTileBytes : kPageBytes);
+        mbar_arrive_expect_tx(full(s), (has1 ? 2 : 1) * (kPageBytes + kPageKeys * 4));
         const uint32_t dst = sbase + L::kOffK + s * kTileBytes;
+        const uint32_t sdst = sbase + L::kOffS + s * kTileKeys * 4;
         long long pg = __ldg(p.block_table + t * p.bt_stride + blk0);
         if (pg < 0 || pg >= p.num_pages) {
           if (p.err) atomicOr(p.err, DSA_DEVERR_SLOT);
           pg = 0;
         }
         tma_load_3d(dst, &tk, 0, 0, static_cast<int>(pg), full(s));
+        bulk_g2s(sdst, p.cache + pg * kPageStride + kPageBytes, kPageKeys * 4, full(s));
         if (has1) {
           pg = __ldg(p.block_table + t * p.bt_stride + blk1);
           if (pg < 0 || pg >= p.num_pages) {
@@ -236,6 +245,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
             pg = 0;
           }
           tma_load_3d(dst + kPageBytes, &tk, 0, 0, static_cast<int>(pg), full(s));
+          bulk_g2s(sdst + kPageKeys * 4, p.cache + pg * kPageStride + kPageBytes, kPageKeys * 4,
+                   full(s));
         }
       }
       if (!ok) {
@@ -292,25 +303,18 @@ __global__ void __launch_bounds__(kLThreads, 1)
     const int sub = warp & 3;               // the TMEM lanes this warp may read
     const int row = 32 * sub + lane;        // key within the tile
     float* out = p.logits + static_cast<long long>(t) * p.logits_stride;
-    // the key scale of this thread's key in tile i (0 past the context)
-    auto key_scale = [&](int i) {
-      const int j = i * kTileKeys + row;
-      if (i >= ntiles || j >= len) return 0.0f;
-      long long pg = __ldg(p.block_table + t * p.bt_stride + j / kPageKeys);
-      if (pg < 0 || pg >= p.num_pages) pg = 0;
-      return __ldg(reinterpret_cast<const float*>(p.cache + pg * kPageStride + kPageBytes) +
-                   (j % kPageKeys));
-    };
+    const float* ssm = reinterpret_cast<const float*>(smem + L::kOffS);
     int m = 0;
     bool ok = true;
-    float ks_next = key_scale(blockIdx.x);
     for (int i = blockIdx.x; i < p.tiles_max; i += gridDim.x) {
       const int j = i * kTileKeys + row;
       if (i < ntiles && ok) {
-        const float ks = ks_next;
-        ks_next = key_scale(i + gridDim.x);   // in flight while this tile is reduced
         const int b = m & 1;
-        const bool got = mbar_wait(accfull(b), (m >> 1) & 1, abort_flag);
+        const int s = m % kKStages;
+        // the stage's scale block landed with its codes; the stage cannot be
+        // refilled before this warp arrives on its "empty" barrier below
+        const bool got = mbar_wait(accfull(b), (m >> 1) & 1, abort_flag) &&
+                         mbar_wait(full(s), (m / kKStages) & 1, abort_flag);
         if (!__all_sync(kFull, got)) {
           ok = false;
           if (lane == 0) {
@@ -320,6 +324,9 @@ __global__ void __launch_bounds__(kLThreads, 1)
           continue;
         }
         tc_fence_after();
+        const float ks = ssm[s * kTileKeys + row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));
         float acc = 0.0f;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * sub) << 16) +
                                static_cast<uint32_t>(b * NH);
@@ -385,7 +392,7 @@ std::mutex g_ldev_mu;
 // the per-block reservation), registers and threads.
 template <int NH>
 cudaError_t prepare_kernel(int dev, int* occ) {
-  const int smem = LSmem<NH>::kBytes + 1024;
+  const int smem = LSmem<NH>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(dsa_mqa_logits_kernel<NH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
@@ -445,7 +452,7 @@ cudaError_t launch_logits(const CUtensorMap& tq, const CUtensorMap& tk, const LP
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kLThreads);
-  cfg.dynamicSmemBytes = LSmem<NH>::kBytes + 1024;
+  cfg.dynamicSmemBytes = LSmem<NH>::kBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   if (pdl) {

@@ -213,15 +213,28 @@ __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params
   long long pos = 0;
   bool pos_ok = false;
   Rot<RP> r;
-  // With DSA_FLAG_PDL_EARLY_ROPE the caller guarantees that positions, slots
-  // and the cos/sin cache are not written by the previous kernel in the
-  // stream, so their two dependent round trips overlap its tail.
   // Let the next kernel of the stream get its CTAs resident now: it waits for
   // this grid's completion on its own griddepcontrol.wait.
   grid_launch_dependents();
-  if (p.early_rope && u < p.q_warps + p.k_warps) pos_ok = token_rot<RP>(p, tt, l, pos, r);
-  grid_dependency_wait();
   if (u >= p.q_warps + p.k_warps) return;  // warp-uniform
+  // Under PDL what follows, up to the wait, runs while the previous kernel of
+  // the stream finishes.  The quarter-warp's input row starts on its way into
+  // L2 (a hint, safe whoever writes the row; see prefetch_l2_bulk).  With
+  // DSA_FLAG_PDL_EARLY_ROPE the caller guarantees that positions, slots and
+  // the cos/sin cache are not written by the previous kernel, so their two
+  // dependent round trips overlap its tail as well.
+  if (l == 0) {
+    if (is_q) {
+      const int v = static_cast<int>(u - t * p.NQ) * 4 + qtr;
+      const int vl = v < p.H ? v : p.H - 1;
+      prefetch_l2_bulk(p.q + t * p.sq_t + vl * p.sq_h, 2 * kD);
+      prefetch_l2(p.w + t * p.sw_t + vl);
+    } else {
+      prefetch_l2_bulk(p.k + tt * p.sk_t, 2 * kD);
+    }
+  }
+  if (p.early_rope) pos_ok = token_rot<RP>(p, tt, l, pos, r);
+  grid_dependency_wait();
 
   if (is_q) {
     const int v = static_cast<int>(u - t * p.NQ) * 4 + qtr;
