@@ -697,9 +697,9 @@ def _logits_inputs(torch, dev, synth, T=64, H=64, context=16384):
                     out=torch.empty((T, li.max_context), dtype=torch.float32, device=dev))
 
 
-def _logits_call(dp, li, t, stream):
+def _logits_call(dp, li, t, stream, pdl=False):
     dp.dsa_indexer_mqa_logits(t["q"], t["w"], t["cache"], li.page_size, t["bt"], t["lens"],
-                              li.max_context, logits=t["out"], stream=stream)
+                              li.max_context, logits=t["out"], stream=stream, pdl=pdl)
 
 
 def _logits_timing(dp, torch, dev, peaks, calls=10, reps=20):
@@ -714,25 +714,32 @@ def _logits_timing(dp, torch, dev, peaks, calls=10, reps=20):
         for _ in range(3):
             _logits_call(dp, li, t, stream)
     stream.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for _ in range(calls):
-            _logits_call(dp, li, t, stream)
-    with torch.cuda.stream(stream):
-        g.replay()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
+
+    def timed(pdl):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(calls):
+                _logits_call(dp, li, t, stream, pdl=pdl)
+        with torch.cuda.stream(stream):
             g.replay()
-        e1.record(stream)
-    stream.synchronize()
-    us = e0.elapsed_time(e1) * 1000.0 / (calls * reps)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) * 1000.0 / (calls * reps)
+
+    us = timed(False)
+    us_pdl = timed(True)
+    us_pdl_early = timed("early")
     T, H, L = li.T, li.H, int(li.context_lens[0])
     nbytes = T * (L * (128 + 4 + 4) + (L // 64) * 4 + H * (128 + 4) + 4)
     flops = 2.0 * T * L * H * 128
     fp8_peak = 2.0 * peaks.get("bf16_tflops", 1900.0)
     return {"workload": f"T={T} H={H} context={L} page_size=64", "us_per_call": us,
+            "us_per_call_pdl": us_pdl, "us_per_call_pdl_early": us_pdl_early,
             "gb_per_s": nbytes / us / 1e3, "hbm_frac": nbytes / us / 1e3 / peaks["hbm_gbs"],
             "tflops": flops / us / 1e6, "fp8_peak_tflops": fp8_peak,
             "fp8_frac": flops / us / 1e6 / fp8_peak,

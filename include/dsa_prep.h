@@ -134,6 +134,13 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
  * orthogonal.  Accepted by dsa_indexer_qk_prepare_store and
  * dsa_indexer_k_prepare_store; the unfused chain rejects it. */
 #define DSA_FLAG_HADAMARD 32u
+/* dsa_indexer_mqa_logits, with DSA_FLAG_PDL only: the caller promises that
+ * block_table and context_lens are NOT written by the kernel that precedes
+ * the call in the stream (true in a decode step, where only q_fp8, the
+ * weights and one cache slot per sequence are).  The kernel then reads them,
+ * and starts its first key pages on their way into L2, before it waits for
+ * that kernel.  The fused prepare-and-store calls reject this flag. */
+#define DSA_FLAG_PDL_EARLY_INDEX 64u
 /* TEST ONLY, with DSA_FLAG_PIPELINE: the producer warp of the pipeline
  * kernel's first CTA withholds the copies of its first unit and never marks
  * that stage full.  That CTA's consumers then give up their bounded waits
@@ -292,7 +299,8 @@ dsa_status dsa_indexer_qk_prepare_store_unfused_noalloc(
  *                  bt_stride: the physical page of each 64-key block.
  *   context_lens   int32 [T], keys of token t.
  *   logits         fp32 [T, logits_stride >= max_context].
- *   T <= 65535; H in {16, 32, 64, 128}; flags may hold DSA_FLAG_PDL.
+ *   T <= 65535; H in {16, 32, 64, 128}; flags may hold DSA_FLAG_PDL and,
+ *   with it, DSA_FLAG_PDL_EARLY_INDEX.
  * Runs on the tensor cores (tcgen05, fp32 accumulation in TMEM); the first
  * call on a device raises its shared-memory limit there.  A block-table entry
  * outside [0, num_pages) sets DSA_DEVERR_SLOT (its keys then read page 0).

@@ -26,7 +26,7 @@ __all__ = [
     "DsaError", "NEOX", "GPTJ", "HEAD_DIM", "DEVERR_POSITION", "DEVERR_SLOT", "DEVERR_TIMEOUT",
     "DEVERR_INTERNAL",
     "FLAG_PDL", "FLAG_PIPELINE", "FLAG_DIRECT", "FLAG_PDL_EARLY_ROPE", "FLAG_CACHE_TOKEN_MAJOR",
-    "FLAG_HADAMARD",
+    "FLAG_HADAMARD", "FLAG_PDL_EARLY_INDEX",
     "dsa_indexer_qk_prepare_store", "dsa_indexer_k_prepare_store", "dsa_status_string",
     "dsa_indexer_qk_prepare_store_unfused", "dsa_unfused_workspace_bytes",
     "dsa_indexer_qk_prepare_store_unfused_noalloc", "dsa_indexer_mqa_logits",
@@ -39,6 +39,7 @@ DEVERR_POSITION, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1, 2, 4, 8
 FLAG_PDL, FLAG_PIPELINE, FLAG_DIRECT, FLAG_PDL_EARLY_ROPE = 1, 2, 4, 8
 FLAG_CACHE_TOKEN_MAJOR = 16
 FLAG_HADAMARD = 32
+FLAG_PDL_EARLY_INDEX = 64
 FLAG_TEST_WITHHOLD_UNIT = 1 << 30  # test only: see include/dsa_prep.h
 _LAYOUT_FLAGS = {"paged": 0, "token_major": FLAG_CACHE_TOKEN_MAJOR}
 _KERNEL_FLAGS = {"auto": 0, "pipeline": FLAG_PIPELINE, "direct": FLAG_DIRECT}
@@ -361,7 +362,11 @@ def dsa_indexer_mqa_logits(q_fp8, weights, index_k_cache, page_size, block_table
     for j < context_lens[t], -inf up to max_context.  q_fp8 [T, H, 128]
     (float8_e4m3fn or uint8), weights [T, H] fp32, index_k_cache page-blocked
     (page_size 64), block_table [T, n] int32, context_lens [T] int32.
+    ``pdl``: False, True, or "early" (PDL plus FLAG_PDL_EARLY_INDEX: the
+    block table and context lengths are not written by the previous kernel).
     Returns logits [T, max_context] fp32."""
+    if pdl not in (False, True, "early"):
+        raise ValueError('pdl must be False, True or "early"')
     if q_fp8.dtype not in (torch.float8_e4m3fn, torch.uint8):
         raise TypeError("q_fp8 must be float8_e4m3fn or uint8 codes")
     if not q_fp8.is_cuda or not q_fp8.is_contiguous() or q_fp8.dim() != 3 \
@@ -380,7 +385,8 @@ def dsa_indexer_mqa_logits(q_fp8, weights, index_k_cache, page_size, block_table
     st = library().dsa_indexer_mqa_logits(
         _ptr(q_fp8), _ptr(weights), _ptr(index_k_cache), _num_pages(index_k_cache, page_size),
         page_size, _ptr(block_table), block_table.stride(0), _ptr(context_lens), _ptr(logits),
-        logits.stride(0), int(max_context), T, H, FLAG_PDL if pdl else 0, _ptr(err_flags),
+        logits.stride(0), int(max_context), T, H,
+        (FLAG_PDL if pdl else 0) | (FLAG_PDL_EARLY_INDEX if pdl == "early" else 0), _ptr(err_flags),
         _stream(stream))
     if st != 0:
         raise DsaError(st, "dsa_indexer_mqa_logits")

@@ -38,6 +38,7 @@ using namespace dsa_dev;
 constexpr int kTileKeys = 128;                  // MMA M: keys per tile
 constexpr int kPageKeys = 64;                   // keys per cache page
 constexpr int kKStages = 4;                     // key-tile ring depth
+constexpr int kBatch = 8;                       // block-table entries fetched ahead, in tiles
 constexpr int kLThreads = 6 * 32;               // producer, MMA, 4 epilogue warps
 constexpr int kTileBytes = kTileKeys * kD;      // 16 KiB of e4m3 codes
 constexpr int kPageBytes = kPageKeys * kD;      // 8 KiB
@@ -55,6 +56,7 @@ struct LParams {
   int max_context;
   int tiles_max;  // ceil(max_context / 128)
   int T;
+  int early_index;  // read context_lens / block_table before the PDL wait
   int* err;
 };
 
@@ -205,11 +207,51 @@ __global__ void __launch_bounds__(kLThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kOffTmem);
 
+  // Page indices come from the block table a batch of kBatch tiles at a
+  // time (the producer keeps the next batch's loads in flight while it
+  // issues this one), so the table's latency is not paid per tile.
+  const int* bt = p.block_table + t * p.bt_stride;
+  const int step = static_cast<int>(gridDim.x);
+  auto load_batch = [&](int i0, int ntiles, int len, int (&pg)[2 * kBatch]) {
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int i = i0 + k * step;
+      pg[2 * k] = i < ntiles ? __ldg(bt + 2 * i) : 0;
+      pg[2 * k + 1] = (i < ntiles && (2 * i + 1) * kPageKeys < len) ? __ldg(bt + 2 * i + 1) : 0;
+    }
+  };
+  auto tiles_of = [](int len) { return len > 0 ? (len + kTileKeys - 1) / kTileKeys : 0; };
+  int cur[2 * kBatch];
+  int len = 0;
+  if (p.early_index) {
+    // DSA_FLAG_PDL_EARLY_INDEX: the context length and the block table are
+    // not written by the previous kernel.  The producer also starts its first
+    // pages on their way into L2 (a hint, coherent with any write the
+    // previous kernel makes to them) while that kernel finishes.
+    len = __ldg(p.context_lens + t);
+    if (warp == 0 && lane == 0) {
+      const int nt = tiles_of(len);
+      load_batch(static_cast<int>(blockIdx.x), nt, len, cur);
+#pragma unroll
+      for (int k = 0; k < kKStages; ++k) {
+        const int i = static_cast<int>(blockIdx.x) + k * step;
+        if (i < nt) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const long long pg = cur[2 * k + h];
+            if ((h == 0 || (2 * i + 1) * kPageKeys < len) && pg >= 0 && pg < p.num_pages)
+              prefetch_l2_bulk(p.cache + pg * kPageStride, kPageStride);
+          }
+        }
+      }
+    }
+  }
+
   grid_dependency_wait();
   grid_launch_dependents();
 
-  const int len = __ldg(p.context_lens + t);
-  const int ntiles = len > 0 ? (len + kTileKeys - 1) / kTileKeys : 0;
+  if (!p.early_index) len = __ldg(p.context_lens + t);
+  const int ntiles = tiles_of(len);
 
   if (warp == 0) {
     // ------------------------------------------------ producer
@@ -220,34 +262,38 @@ __global__ void __launch_bounds__(kLThreads, 1)
         mbar_arrive_expect_tx(qfull, L::kQBytes);
         tma_load_2d(sbase + L::kOffQ, &tq, 0, t * NH, qfull);
       }
-      for (int i = blockIdx.x; i < ntiles; i += gridDim.x, ++m) {
-        const int s = m % kKStages;
-        if (m >= kKStages && !mbar_wait(empty(s), ((m / kKStages) & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const int blk0 = 2 * i, blk1 = 2 * i + 1;
-        const bool has1 = blk1 * kPageKeys < len;
-        mbar_arrive_expect_tx(full(s), (has1 ? 2 : 1) * (kPageBytes + kPageKeys * 4));
-        const uint32_t dst = sbase + L::kOffK + s * kTileBytes;
-        const uint32_t sdst = sbase + L::kOffS + s * kTileKeys * 4;
-        long long pg = __ldg(p.block_table + t * p.bt_stride + blk0);
-        if (pg < 0 || pg >= p.num_pages) {
-          if (p.err) atomicOr(p.err, DSA_DEVERR_SLOT);
-          pg = 0;
-        }
-        tma_load_3d(dst, &tk, 0, 0, static_cast<int>(pg), full(s));
-        bulk_g2s(sdst, p.cache + pg * kPageStride + kPageBytes, kPageKeys * 4, full(s));
-        if (has1) {
-          pg = __ldg(p.block_table + t * p.bt_stride + blk1);
-          if (pg < 0 || pg >= p.num_pages) {
-            if (p.err) atomicOr(p.err, DSA_DEVERR_SLOT);
-            pg = 0;
+      int nxt[2 * kBatch];
+      if (!p.early_index) load_batch(static_cast<int>(blockIdx.x), ntiles, len, cur);
+      for (int i0 = blockIdx.x; ok && i0 < ntiles; i0 += kBatch * step) {
+        load_batch(i0 + kBatch * step, ntiles, len, nxt);
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int i = i0 + k * step;
+          if (!ok || i >= ntiles) break;
+          const int s = m % kKStages;
+          if (m >= kKStages && !mbar_wait(empty(s), ((m / kKStages) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
           }
-          tma_load_3d(dst + kPageBytes, &tk, 0, 0, static_cast<int>(pg), full(s));
-          bulk_g2s(sdst + kPageKeys * 4, p.cache + pg * kPageStride + kPageBytes, kPageKeys * 4,
-                   full(s));
+          const bool has1 = (2 * i + 1) * kPageKeys < len;
+          mbar_arrive_expect_tx(full(s), (has1 ? 2 : 1) * (kPageBytes + kPageKeys * 4));
+          const uint32_t dst = sbase + L::kOffK + s * kTileBytes;
+          const uint32_t sdst = sbase + L::kOffS + s * kTileKeys * 4;
+          auto load_page = [&](int h, long long pg) {
+            if (pg < 0 || pg >= p.num_pages) {
+              if (p.err) atomicOr(p.err, DSA_DEVERR_SLOT);
+              pg = 0;
+            }
+            tma_load_3d(dst + h * kPageBytes, &tk, 0, 0, static_cast<int>(pg), full(s));
+            bulk_g2s(sdst + h * kPageKeys * 4, p.cache + pg * kPageStride + kPageBytes,
+                     kPageKeys * 4, full(s));
+          };
+          load_page(0, cur[2 * k]);
+          if (has1) load_page(1, cur[2 * k + 1]);
+          ++m;
         }
+#pragma unroll
+        for (int k = 0; k < 2 * kBatch; ++k) cur[k] = nxt[k];
       }
       if (!ok) {
         *abort_flag = 1;
@@ -479,7 +525,9 @@ dsa_status dsa_indexer_mqa_logits(const void* q_fp8, const float* weights,
     return DSA_ERR_SHAPE;
   if (H != 16 && H != 32 && H != 64 && H != 128) return DSA_ERR_UNSUPPORTED;
   if (page_size != kPageKeys) return DSA_ERR_UNSUPPORTED;
-  if (flags & ~static_cast<uint32_t>(DSA_FLAG_PDL)) return DSA_ERR_UNSUPPORTED;
+  if (flags & ~static_cast<uint32_t>(DSA_FLAG_PDL | DSA_FLAG_PDL_EARLY_INDEX))
+    return DSA_ERR_UNSUPPORTED;
+  if ((flags & DSA_FLAG_PDL_EARLY_INDEX) && !(flags & DSA_FLAG_PDL)) return DSA_ERR_UNSUPPORTED;
   if (num_pages > 0x7fffffffLL || static_cast<long long>(T) * H > 0x7fffffffLL)
     return DSA_ERR_SHAPE;
   if (logits_stride < max_context) return DSA_ERR_SHAPE;
@@ -536,6 +584,7 @@ dsa_status dsa_indexer_mqa_logits(const void* q_fp8, const float* weights,
   p.max_context = max_context;
   p.tiles_max = (max_context + kTileKeys - 1) / kTileKeys;
   p.T = T;
+  p.early_index = (flags & DSA_FLAG_PDL_EARLY_INDEX) ? 1 : 0;
   p.err = err_flags;
   // split each token's tiles over as many CTAs as fit on the GPU at once
   // (all resident: no second wave), at least one per token

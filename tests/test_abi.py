@@ -131,3 +131,25 @@ def test_unfused_validation(lib, over, status):
 
 def test_unfused_empty_batch(lib):
     assert _unf(lib, T=0, q=None, k=None, ws=None, wsb=0) == 0
+
+
+def _lg(lib, **over):
+    args = dict(q=A, w=A, cache=A, pages=4, ps=64, bt=A, bts=4, lens=A, out=A, outs=128,
+                maxc=128, T=2, H=64, flags=0, err=None, stream=None)
+    args.update(over)
+    return lib.dsa_indexer_mqa_logits(*args.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(T=-1), 3), (dict(T=70000), 3), (dict(H=48), 4), (dict(ps=32), 4), (dict(pages=0), 3),
+    (dict(bts=-1), 3), (dict(outs=64), 3), (dict(flags=2), 4), (dict(flags=128), 4),
+    (dict(flags=64), 4),  # DSA_FLAG_PDL_EARLY_INDEX needs DSA_FLAG_PDL
+    (dict(q=None), 1), (dict(lens=None), 1), (dict(q=A + 8), 2), (dict(cache=A + 4), 2),
+    (dict(w=A + 2), 2),
+])
+def test_logits_validation(lib, over, status):
+    assert _lg(lib, **over) == status
+
+
+def test_logits_empty_batch_is_ok_without_pointers(lib):
+    assert _lg(lib, T=0, q=None, w=None, bt=None, lens=None, out=None) == 0

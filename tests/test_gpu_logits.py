@@ -109,3 +109,33 @@ def test_bad_page_sets_error_bit():
     ref = _oracle(li, [0])
     fin = np.isfinite(ref)
     assert np.all(np.abs(got[0][fin[0]] - ref[0][fin[0]]) <= _tolerance(li, [0])[0][fin[0]] + 1e-30)
+
+
+@pytest.mark.parametrize("pdl", [True, "early"])
+def test_pdl_graph_matches_eager(pdl):
+    """A graph of PDL launches (with early reads of the block table and the
+    context lengths, which no kernel in the graph writes) gives the eager
+    bytes."""
+    import prep_token_gb300 as dp
+    li = synth.make_logits(seed=11, T=8, H=64, context=1000, ragged=True)
+    eager = _run_gpu(li)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    q, w, cache, bt, lens = d(li.q_fp8), d(li.weights), d(li.cache), d(li.block_table), d(li.context_lens)
+    out = torch.full((li.T, li.max_context), 7.0, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dp.dsa_indexer_mqa_logits(q, w, cache, li.page_size, bt, lens, li.max_context,
+                                  logits=out, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            dp.dsa_indexer_mqa_logits(q, w, cache, li.page_size, bt, lens, li.max_context,
+                                      logits=out, pdl=pdl, stream=s)
+    out.fill_(7.0)
+    g.replay()
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.array_equal(np.isneginf(got), np.isneginf(eager))
+    fin = np.isfinite(eager)
+    assert np.array_equal(got[fin], eager[fin])
