@@ -33,7 +33,8 @@ kernel launch.  Prints ONE JSON line (rank 0):
              cache) on the tcgen05 tensor cores at the 16K-context decode step
   cpu_baseline  the oracle (plain C) on a bounded sample, one spawned process
              per host core over disjoint token ranges; the one-core figure
-             sits inside it
+             sits inside it, and so do one-core us/call figures for the
+             tiny, decode and sweep workloads
 
 ``--impl reference`` times the oracle instead (the CPU statement of the path),
 on the same workload and metric.
@@ -484,6 +485,7 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(sets[0][0], budget_s=args.cpu_seconds)
         cpu = cpu_baseline_parallel(sets[0][0], cpu, budget_s=args.cpu_seconds)
+        cpu["other_workloads"] = cpu_baseline_configs()
 
     if rank != 0:
         return None
@@ -601,6 +603,31 @@ class OraclePool:
     def close(self):
         self.pool.close()
         self.pool.join()
+
+
+def cpu_baseline_configs(budget_s=0.5):
+    """The oracle on one host core for each of the other workloads (tiny,
+    the decode step, the decode sweep): us per call, each timed over about
+    `budget_s` of repeated calls."""
+    import synth
+    import oracle
+    oracle.build()
+    cases = [("tiny_T4_H8", synth.make_tiny(seed=0, fused_kw=True)),
+             ("c2_decode_T64_H64_gptj", synth.make_decode(seed=1))]
+    cases += [(f"sweep_T{n}_H32", synth.make_sweep(n, seed=2)) for n in (1, 8, 32, 64, 256)]
+    out = {}
+    for name, inp in cases:
+        cache = np.zeros(inp.cache_bytes, np.uint8)
+        q_fp8 = np.zeros((inp.T, inp.H, 128), np.uint8)
+        weights = np.zeros((inp.T, inp.H), np.float32)
+        calls, t0 = 0, time.perf_counter()
+        while calls == 0 or time.perf_counter() - t0 < budget_s:
+            _oracle_call(inp, 0, inp.T, cache, q_fp8, weights)
+            calls += 1
+        us = (time.perf_counter() - t0) / calls * 1e6
+        out[name] = {"us_per_call": us, "tokens_per_s": inp.T / (us * 1e-6), "calls": calls,
+                     "cores": 1}
+    return out
 
 
 def cpu_baseline_parallel(inp, single, budget_s=10.0):
