@@ -131,3 +131,58 @@ def test_scores_match_the_plain_path():
     bound = 2.0 * (2 * 2.0 ** -4 + 2.0 ** -8) * 1.1 * mass
     assert np.all(np.abs(rot - plain) <= bound)
     assert np.corrcoef(rot.ravel(), plain.ravel())[0, 1] > 0.99
+
+
+@pytest.mark.parametrize("style", [synth.NEOX, synth.GPTJ])
+def test_stress_full_size(style):
+    """The heavy-tailed stress set (8 sequences x 8192 tokens, Student-t
+    values, all-zero rows, planted near-ties, shuffled pages) at full size."""
+    inp = synth.make_stress(style=style)
+    _check(inp, kernels=("pipeline",))
+
+
+@pytest.mark.parametrize("T,H", [(1, 1), (1, 128), (2, 3)])
+def test_smallest_shapes(T, H):
+    _check(synth.make_decode(seed=100 + T * 7 + H, T=T, H=H, style=(T + H) % 2))
+
+
+@pytest.mark.parametrize("pdl", [True, "early"])
+def test_pdl_graph_of_layers_matches_eager(pdl):
+    """Three layers' calls in one CUDA graph with PDL (the second and third
+    start while the one before drains): every layer's bytes equal its eager
+    call's."""
+    import prep_token_gb300 as dp
+    layers = [synth.make_decode(seed=110 + i, T=64, H=16) for i in range(3)]
+    for inp in layers[1:]:
+        inp.positions, inp.slots = layers[0].positions, layers[0].slots
+        inp.cos, inp.sin, inp.max_position = layers[0].cos, layers[0].sin, layers[0].max_position
+    devs = [to_device(inp) for inp in layers]
+    eager = [run_qk(inp, d, hadamard=True) for inp, d in zip(layers, devs)]
+    caches = [new_cache(inp) for inp in layers]
+    outs = [(torch.empty((64, 16, 128), dtype=torch.float8_e4m3fn, device="cuda"),
+             torch.empty((64, 16), dtype=torch.float32, device="cuda")) for _ in layers]
+
+    def call(inp, d, cache, out, s, pdl_mode):
+        dp.dsa_indexer_qk_prepare_store(
+            d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
+            d["beta"], inp.eps, inp.softmax_scale, cache, inp.page_size, inp.rope_dim,
+            inp.style, q_fp8_out=out[0], weights_out=out[1], max_position=inp.max_position,
+            pdl=pdl_mode, hadamard=True, stream=s)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for args in zip(layers, devs, caches, outs):
+            call(*args, s, False)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for args in zip(layers, devs, caches, outs):
+            call(*args, s, pdl)
+    for c in caches:
+        c.fill_(0xCD)
+    g.replay()
+    torch.cuda.synchronize()
+    for e, c, (qo, wo) in zip(eager, caches, outs):
+        assert np.array_equal(qo.view(torch.uint8).cpu().numpy(), e["q_fp8"])
+        assert np.array_equal(wo.cpu().numpy(), e["weights"])
+        assert np.array_equal(c.cpu().numpy(), e["cache"])
