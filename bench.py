@@ -454,6 +454,14 @@ def run_ours(args, rank, world, local_rank):
                    "hbm_bytes_per_call": synth.algorithmic_bytes(T, H)
                    + T * (H + 1) * 128 * 2 * 2 + T * 128 * 2 * 2}
 
+    # the same launches under programmatic dependent launch: a launch's CTAs
+    # start on SMs the previous one has left and wait there for it to finish
+    pdl_us, pdl_calls = _prefill_graph_us(
+        torch, sets, stream, lambda inp, d: _call(dp, inp, d, stream, pdl=True), args.steps)
+    prefill_pdl = {"us_per_call": pdl_us, "calls": pdl_calls,
+                   "gb_per_s": algo_bytes / (pdl_us * 1e-6) / 1e9,
+                   "hbm_frac": algo_bytes / (pdl_us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+
     # the Hadamard-rotated variant: same bytes, more arithmetic per vector
     hadamard = None
     if not args.no_hadamard:
@@ -526,6 +534,7 @@ def run_ours(args, rank, world, local_rank):
         "decode": decode,
         "unfused": unfused,
         "hadamard": hadamard,
+        "prefill_pdl": prefill_pdl,
         "mqa_logits": logits,
         "cpu_baseline": cpu,
     }
