@@ -45,7 +45,8 @@
  *     contiguous.
  *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  No call synchronises the host, so every call can be
- *     captured into a CUDA graph.  One kernel launch per call.  The first call
+ *     captured into a CUDA graph.  One kernel launch per call (the unfused
+ *     comparison chain: four).  The first call
  *     on a device raises the kernel's dynamic shared-memory limit there (a
  *     per-device, once-only setting); make it before capturing a graph.
  *   - Host-side checks: a bad argument returns a status other than DSA_OK and
@@ -167,8 +168,8 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
  *   cos_cache,     fp32 [max_position, >= rope_dim/2] each, row stride
  *   sin_cache      cs_stride (multiple of 4); 16-byte aligned.  May be NULL
  *                  when rope_dim == 0.
- *   ln_gamma,      fp32 [128], 16-byte aligned; ln_eps > 0 (it sits inside
- *   ln_beta        the square root).
+ *   ln_gamma,      fp32 [128], 16-byte aligned; ln_eps finite and >= 0 (it
+ *   ln_beta        sits inside the square root).
  *   softmax_scale  the caller's attention scale (DeepSeek-style indexers pass
  *                  128^-0.5); H^-0.5 is applied here.
  *   q_fp8_out      e4m3 bytes [T, H, 128], contiguous, 16-byte aligned.
