@@ -420,20 +420,24 @@ __device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t 
       load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(sts + kOffSin + 4 * RP * l, r.s);
       finish_rot<RP>(r);
     }
+    // Per-unit bases, so a head costs a few 32-bit offsets: its output rows,
+    // and its gate weights -- in the stage when they rode the bulk copy, else
+    // in global memory; one generic pointer serves both.
     const long long orow0 = t * p.H + h0;
+    uint8_t* const q_out = p.q_out + orow0 * kD;
+    float* const w_out = p.w_out + orow0;
+    const uint16_t* const w_src =
+        p.w_bulk ? reinterpret_cast<const uint16_t*>(st + kOffW) : p.w + t * p.sw_t + h0;
+    const bool w_lane = pos_ok && l == 0;
     // One query head of the chunk for this quarter-warp: head v (a quarter-
     // warp past the chunk's last head re-reads it and stores nothing).
     auto q_head = [&](int v, float (&x)[16]) {
       const bool valid = v < n;
       const int vl = valid ? v : n - 1;
       load_vec<HAD, STYLE, RP, SharedMem>(sts + kOffQ + 256 * vl, l, x);
-      const float wv =
-          p.w_bulk ? __uint_as_float(static_cast<uint32_t>(
-                         *reinterpret_cast<const uint16_t*>(st + kOffW + 2 * vl)) << 16)
-                   : __uint_as_float(static_cast<uint32_t>(__ldg(p.w + t * p.sw_t + h0 + vl)) << 16);
-      const int e = q_slice<HAD, STYLE, RP>(x, r, p.q_out + (orow0 + v) * kD, l, valid && pos_ok);
-      store_f32_cs(p.w_out + orow0 + v, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold),
-                   valid && pos_ok && l == 0);
+      const float wv = __uint_as_float(static_cast<uint32_t>(w_src[vl]) << 16);
+      const int e = q_slice<HAD, STYLE, RP>(x, r, q_out + v * kD, l, valid && pos_ok);
+      store_f32_cs(w_out + v, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold), valid && w_lane);
     };
     // query heads: warp cw takes head quads cw, cw + kConsumers, ...
     for (int qd = cw; 4 * qd < n; qd += kConsumers) {
