@@ -29,6 +29,8 @@ kernel launch.  Prints ONE JSON line (rank 0):
   unfused    the same call as four launches with bf16 intermediates (the
              pages' pre-fusion chain) on the prefill inputs and in the decode
              step, for the 4 -> 1 launch comparison
+  stress     the heavy-tailed 65,536-token workload (1.7 GB per call) in
+             both pairings: us/call and HBM GB/s
   mqa_logits the indexer's fp8 paged MQA logits (the consumer of the index-K
              cache) on the tcgen05 tensor cores at the 16K-context decode step
   cpu_baseline  the oracle (plain C) on a bounded sample, one spawned process
@@ -476,6 +478,26 @@ def run_ours(args, rank, world, local_rank):
             hadamard["c2_decode_T64_H64_gptj"] = _decode_timings(
                 dp, torch, dev, lambda i: synth.make_decode(seed=1 + 100 * i), hadamard=True)
 
+    # the heavy-tailed stress workload at full size: 8 sequences x 8192 tokens,
+    # 1.7 GB per call (far larger than L2), in both pairings
+    stress = None
+    if not args.no_stress:
+        sinp = synth.make_stress(seed=4 + 1000 * rank)
+        sd = _dev_inputs(sinp, dev)
+        sbytes = synth.algorithmic_bytes(sinp.T, sinp.H)
+        stress = {"workload": f"T={sinp.T} H={sinp.H} (8 x 8192 tokens) rope_dim=64, "
+                              f"2048 shuffled pages", "algorithmic_bytes": sbytes}
+        for style, name in ((synth.NEOX, "neox"), (synth.GPTJ, "gptj")):
+            sinp.style = style
+            us, calls = _prefill_graph_us(torch, [(sinp, sd), (sinp, sd)], stream,
+                                          lambda inp, d: _call(dp, inp, d, stream),
+                                          min(args.steps, 200))
+            gbs = sbytes / (us * 1e-6) / 1e9
+            stress[name] = {"us_per_call": us, "calls": calls, "gb_per_s": gbs,
+                            "hbm_frac": gbs / peaks["hbm_gbs"],
+                            "tokens_per_s": sinp.T / (us * 1e-6)}
+        del sd
+
     logits = None
     if rank == 0 and not args.no_logits:
         logits = _logits_timing(dp, torch, dev, peaks)
@@ -535,6 +557,7 @@ def run_ours(args, rank, world, local_rank):
         "unfused": unfused,
         "hadamard": hadamard,
         "prefill_pdl": prefill_pdl,
+        "stress": stress,
         "mqa_logits": logits,
         "cpu_baseline": cpu,
     }
@@ -819,6 +842,7 @@ def main():
     ap.add_argument("--no-unfused", action="store_true")
     ap.add_argument("--no-logits", action="store_true")
     ap.add_argument("--no-hadamard", action="store_true")
+    ap.add_argument("--no-stress", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--probe", choices=("prefill", "decode", "logits", "prefill_hadamard",
                                         "decode_hadamard"),
