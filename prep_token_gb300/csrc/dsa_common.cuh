@@ -769,6 +769,60 @@ __device__ __forceinline__ void store_index_k_h(const CacheGeom& g, long long sl
   }
 }
 
+// gamma and beta of the lane's 16 elements, in register order, loaded all at
+// once (for latency-bound callers: the loads overlap the LayerNorm sums).
+template <int STYLE, int RP>
+__device__ __forceinline__ void load_affine_slice(const float* gamma, const float* beta, int l,
+                                                  float (&g)[16], float (&b)[16]) {
+  using S = Slice<STYLE, RP>;
+  if constexpr (RP > 0) {
+    if constexpr (S::NEOX) {
+      load_f32_global<RP, S::ALIGN_A_F32>(gamma + RP * l, g);
+      load_f32_global<RP, S::ALIGN_A_F32>(beta + RP * l, b);
+      load_f32_global<RP, S::ALIGN_B_F32>(gamma + S::B_BASE + RP * l, g + RP);
+      load_f32_global<RP, S::ALIGN_B_F32>(beta + S::B_BASE + RP * l, b + RP);
+    } else {
+      float tg[2 * RP], tb[2 * RP];
+      load_f32_global<2 * RP, S::ALIGN_A_F32>(gamma + 2 * RP * l, tg);
+      load_f32_global<2 * RP, S::ALIGN_A_F32>(beta + 2 * RP * l, tb);
+#pragma unroll
+      for (int j = 0; j < RP; ++j) {
+        g[j] = tg[2 * j], g[RP + j] = tg[2 * j + 1];
+        b[j] = tb[2 * j], b[RP + j] = tb[2 * j + 1];
+      }
+    }
+  }
+  if constexpr (S::NP > 0) {
+    load_f32_global<S::NP, S::ALIGN_P_F32>(gamma + S::P_BASE + S::NP * l, g + 2 * RP);
+    load_f32_global<S::NP, S::ALIGN_P_F32>(beta + S::P_BASE + S::NP * l, b + 2 * RP);
+  }
+}
+
+template <int STYLE, int RP>
+__device__ __forceinline__ void load_affine_hslice(const float* gamma, const float* beta, int l,
+                                                   float (&g)[16], float (&b)[16]) {
+  using S = HSlice<STYLE, RP>;
+  constexpr int PIECE = S::W < 4 ? S::W : 4;
+#pragma unroll
+  for (int c = 0; c < S::NCH; ++c)
+#pragma unroll
+    for (int i0 = 0; i0 < S::W; i0 += PIECE) {
+      const int o = c * S::STRIDE + S::W * l + i0;
+      float tg[PIECE], tb[PIECE];
+      load_f32_global<PIECE, 4 * PIECE>(gamma + o, tg);
+      load_f32_global<PIECE, 4 * PIECE>(beta + o, tb);
+#pragma unroll
+      for (int i = 0; i < PIECE; ++i) g[S::reg(c, i0 + i)] = tg[i], b[S::reg(c, i0 + i)] = tb[i];
+    }
+}
+
+// y = x * rstd * gamma + beta with gamma and beta already in registers.
+__device__ __forceinline__ void apply_affine(float (&x)[16], float rstd, const float (&g)[16],
+                                             const float (&b)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) x[j] = __fmaf_rn(__fmul_rn(x[j], rstd), g[j], b[j]);
+}
+
 // bf16 of x, round to nearest even (two at a time): lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

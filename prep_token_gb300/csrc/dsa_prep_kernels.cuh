@@ -127,10 +127,20 @@ __device__ __forceinline__ void raise_error(const Params& p, int bit) {
 
 // Key vector: LayerNorm (mean, biased variance, eps inside the root), RoPE
 // (then H_128 / sqrt(128) in the Hadamard variant), quantise, and store the
-// codes and the scale into slot `slot` of the cache.
-template <bool HAD, int STYLE, int RP>
+// codes and the scale into slot `slot` of the cache.  EARLY_AFFINE loads all
+// of the lane's gamma and beta before the sums, so their latency overlaps
+// them (for the latency-bound decode kernel); otherwise they are loaded piece
+// by piece after the sums, which keeps fewer registers live.
+template <bool HAD, int STYLE, int RP, bool EARLY_AFFINE = false>
 __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const Rot<RP>& r,
                                         int l, bool real, bool pos_ok, long long slot) {
+  float ga[16], be[16];  // used only with EARLY_AFFINE
+  if constexpr (EARLY_AFFINE) {
+    if constexpr (HAD)
+      load_affine_hslice<STYLE, RP>(p.gamma, p.beta, l, ga, be);
+    else
+      load_affine_slice<STYLE, RP>(p.gamma, p.beta, l, ga, be);
+  }
   float sum = 0.0f;
 #pragma unroll
   for (int j = 0; j < 16; ++j) sum = __fadd_rn(sum, x[j]);
@@ -143,7 +153,9 @@ __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const R
   }
   const float var = __fmul_rn(quad_sum(sq), 1.0f / kD);
   const float rstd = __frsqrt_rn(__fadd_rn(var, p.eps));
-  if constexpr (HAD)
+  if constexpr (EARLY_AFFINE)
+    apply_affine(x, rstd, ga, be);
+  else if constexpr (HAD)
     affine_hslice<STYLE, RP>(p.gamma, p.beta, l, x, rstd);
   else
     affine_slice<STYLE, RP>(p.gamma, p.beta, l, x, rstd);
@@ -231,6 +243,10 @@ __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params
       prefetch_l2(p.w + t * p.sw_t + vl);
     } else {
       prefetch_l2_bulk(p.k + tt * p.sk_t, 2 * kD);
+      if (qtr == 0) {
+        prefetch_l2_bulk(p.gamma, 4 * kD);
+        prefetch_l2_bulk(p.beta, 4 * kD);
+      }
     }
   }
   if (p.early_rope) pos_ok = token_rot<RP>(p, tt, l, pos, r);
@@ -255,7 +271,7 @@ __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params
     load_vec<HAD, STYLE, RP, GlobalMem>(reinterpret_cast<const unsigned char*>(p.k + tt * p.sk_t), l, x);
     const long long slot = __ldg(p.loc + tt);
     if (!p.early_rope) pos_ok = token_rot<RP>(p, tt, l, pos, r);
-    k_slice<HAD, STYLE, RP>(p, x, r, l, real, pos_ok, slot);
+    k_slice<HAD, STYLE, RP, true>(p, x, r, l, real, pos_ok, slot);
   }
 }
 
