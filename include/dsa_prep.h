@@ -296,9 +296,11 @@ dsa_status dsa_indexer_qk_prepare_store_unfused_noalloc(
  *   q_fp8          e4m3 [T, H, 128] contiguous, 16-byte aligned.
  *   weights        fp32 [T, H] contiguous.
  *   index_k_cache  page-blocked layout, page_size == 64, 16-byte aligned.
- *   block_table    int32 [T, >= ceil(context_lens[t] / 64)], row stride
- *                  bt_stride: the physical page of each 64-key block.
- *   context_lens   int32 [T], keys of token t.
+ *   block_table    int32 [T, >= ceil(min(context_lens[t], max_context) / 64)],
+ *                  row stride bt_stride: the physical page of each 64-key
+ *                  block.
+ *   context_lens   int32 [T], keys of token t; only the first max_context
+ *                  of them have a column (a longer context is clamped).
  *   logits         fp32 [T, logits_stride >= max_context].
  *   T <= 65535; H in {16, 32, 64, 128}; flags may hold DSA_FLAG_PDL and,
  *   with it, DSA_FLAG_PDL_EARLY_INDEX.

@@ -121,16 +121,21 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
-def _need(t: torch.Tensor, name: str, dtype, dim: int | None = None):
+def _need(t: torch.Tensor, name: str, dtype, dim: int | None = None, device=None):
+    """dtype (one torch dtype or a tuple of them), rank, a CUDA device (the
+    given one when `device` is set) and a contiguous innermost dimension."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must live on a CUDA device (no CPU path)")
-    if t.dtype != dtype:
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the other tensors on {device}")
+    if t.dtype is not dtype and not (isinstance(dtype, tuple) and t.dtype in dtype):
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
-    if dim is not None and t.dim() != dim:
+    nd = t.dim()
+    if dim is not None and nd != dim:
         raise ValueError(f"{name}: expected {dim} dims, got {tuple(t.shape)}")
-    if t.dim() and t.stride(-1) != 1 and t.shape[-1] > 1:
+    if nd and t.stride(-1) != 1 and t.shape[-1] > 1:
         raise ValueError(f"{name}: innermost dimension must be contiguous")
 
 
@@ -162,9 +167,19 @@ def _flags(pdl, kernel: str) -> int:
     return f | _KERNEL_FLAGS[kernel]
 
 
-def _stream(stream) -> int:
+def _err_ptr(err_flags, device):
+    """The device error word: an int32 CUDA tensor on the call's device."""
+    if err_flags is None:
+        return None
+    _need(err_flags, "err_flags", torch.int32, None, device)
+    if err_flags.numel() < 1:
+        raise ValueError("err_flags must hold at least one int32")
+    return err_flags.data_ptr()
+
+
+def _stream(stream, device=None) -> int:
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        return torch.cuda.current_stream(device).cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
     return int(stream)
@@ -173,15 +188,16 @@ def _stream(stream) -> int:
 def _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta,
               index_k_cache, rope_dim):
     _need(k, "k", torch.bfloat16, 2)
-    _need(positions, "positions", torch.int64, 1)
-    _need(out_cache_loc, "out_cache_loc", torch.int64, 1)
-    _need(ln_gamma, "ln_gamma", torch.float32, 1)
-    _need(ln_beta, "ln_beta", torch.float32, 1)
-    if not isinstance(index_k_cache, torch.Tensor) or not index_k_cache.is_cuda:
-        raise ValueError("index_k_cache must be a CUDA tensor")
+    dev = k.device
+    _need(positions, "positions", torch.int64, 1, dev)
+    _need(out_cache_loc, "out_cache_loc", torch.int64, 1, dev)
+    _need(ln_gamma, "ln_gamma", torch.float32, 1, dev)
+    _need(ln_beta, "ln_beta", torch.float32, 1, dev)
+    if not isinstance(index_k_cache, torch.Tensor) or index_k_cache.device != dev:
+        raise ValueError(f"index_k_cache must be a tensor on {dev}")
     if rope_dim:
-        _need(cos_cache, "cos_cache", torch.float32, 2)
-        _need(sin_cache, "sin_cache", torch.float32, 2)
+        _need(cos_cache, "cos_cache", torch.float32, 2, dev)
+        _need(sin_cache, "sin_cache", torch.float32, 2, dev)
         if cos_cache.stride(0) != sin_cache.stride(0) or cos_cache.shape[0] != sin_cache.shape[0]:
             raise ValueError("cos_cache and sin_cache must share rows and row stride")
         return cos_cache.stride(0), cos_cache.shape[0]
@@ -194,9 +210,12 @@ def _qk_args(q, k, w, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, 
     """Checks and the C argument list shared by the fused and unfused calls,
     up to and including rope_style; also returns the two outputs."""
     _need(q, "q", torch.bfloat16, 3)
-    _need(w, "w", torch.bfloat16, 2)
+    dev = q.device
+    _need(w, "w", torch.bfloat16, 2, dev)
     cs_stride, rows = _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
                                 ln_beta, index_k_cache, rope_dim)
+    if k.device != dev:
+        raise ValueError(f"k is on {k.device}, q on {dev}")
     T = q.shape[0] if num_tokens is None else int(num_tokens)
     H = q.shape[1]
     if q.shape[2] != HEAD_DIM:
@@ -206,15 +225,15 @@ def _qk_args(q, k, w, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, 
             raise ValueError(f"{name} has fewer than {T} rows")
     if w.shape[1] != H:
         raise ValueError("w must be [T, H]")
-    dev = q.device
     if q_fp8_out is None:
         q_fp8_out = torch.empty((T, H, HEAD_DIM), dtype=torch.float8_e4m3fn, device=dev)
     if weights_out is None:
         weights_out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _need(q_fp8_out, "q_fp8_out", (torch.float8_e4m3fn, torch.uint8), None, dev)
+    _need(weights_out, "weights_out", torch.float32, None, dev)
     if q_fp8_out.numel() < T * H * HEAD_DIM or not q_fp8_out.is_contiguous():
         raise ValueError("q_fp8_out must be contiguous [T, H, 128]")
-    if weights_out.dtype != torch.float32 or not weights_out.is_contiguous() \
-            or weights_out.numel() < T * H:
+    if not weights_out.is_contiguous() or weights_out.numel() < T * H:
         raise ValueError("weights_out must be contiguous fp32 [T, H]")
     max_position = rows if max_position is None else int(max_position)
     args = (_ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), _ptr(w), w.stride(0),
@@ -223,8 +242,9 @@ def _qk_args(q, k, w, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, 
             _ptr(ln_beta), float(ln_eps), float(softmax_scale), _ptr(q_fp8_out),
             _ptr(weights_out), _ptr(index_k_cache), _num_pages(index_k_cache, page_size),
             page_size, T, H, HEAD_DIM, rope_dim, int(rope_style))
-    outs = (q_fp8_out[:T] if q_fp8_out.dim() == 3 else q_fp8_out,
-            weights_out[:T] if weights_out.dim() == 2 else weights_out)
+    outs = (q_fp8_out[:T] if q_fp8_out.dim() == 3 and q_fp8_out.shape[0] != T else q_fp8_out,
+            weights_out[:T] if weights_out.dim() == 2 and weights_out.shape[0] != T
+            else weights_out)
     return args, outs, T, H
 
 
@@ -259,7 +279,7 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
                                 num_tokens, max_position)
     st = library().dsa_indexer_qk_prepare_store(
         *args, _flags(pdl, kernel) | _layout(cache_layout) | (FLAG_HADAMARD if hadamard else 0),
-        _ptr(err_flags), _stream(stream))
+        _err_ptr(err_flags, q.device), _stream(stream, q.device))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store")
     return outs
@@ -288,12 +308,13 @@ def dsa_indexer_qk_prepare_store_unfused(q, k, w, positions, out_cache_loc, cos_
     need = dsa_unfused_workspace_bytes(T, H)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    if not workspace.is_cuda or not workspace.is_contiguous():
-        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if not isinstance(workspace, torch.Tensor) or workspace.device != q.device \
+            or not workspace.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {q.device}")
     nbytes = workspace.numel() * workspace.element_size()
     st = library().dsa_indexer_qk_prepare_store_unfused(
         *args, (FLAG_PDL if pdl else 0) | _layout(cache_layout), _ptr(workspace), nbytes,
-        _ptr(err_flags), _stream(stream))
+        _err_ptr(err_flags, q.device), _stream(stream, q.device))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store_unfused")
     return outs
@@ -320,8 +341,8 @@ def dsa_indexer_qk_prepare_store_unfused_noalloc(q, k, w, positions, out_cache_l
                                 page_size, rope_dim, rope_style, q_fp8_out, weights_out,
                                 num_tokens, max_position)
     st = library().dsa_indexer_qk_prepare_store_unfused_noalloc(
-        *args, (FLAG_PDL if pdl else 0) | _layout(cache_layout), _ptr(err_flags),
-        _stream(stream))
+        *args, (FLAG_PDL if pdl else 0) | _layout(cache_layout), _err_ptr(err_flags, q.device),
+        _stream(stream, q.device))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store_unfused_noalloc")
     return outs
@@ -350,7 +371,7 @@ def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cach
         _ptr(index_k_cache), _num_pages(index_k_cache, page_size), page_size, T, HEAD_DIM,
         rope_dim, int(rope_style),
         _flags(pdl, kernel) | _layout(cache_layout) | (FLAG_HADAMARD if hadamard else 0),
-        _ptr(err_flags), _stream(stream))
+        _err_ptr(err_flags, k.device), _stream(stream, k.device))
     if st != 0:
         raise DsaError(st, "dsa_indexer_k_prepare_store")
 
@@ -361,7 +382,10 @@ def dsa_indexer_mqa_logits(q_fp8, weights, index_k_cache, page_size, block_table
     logits[t, j] = k_scale[j] * sum_h weights[t, h] * relu(q[t, h] . k[j])
     for j < context_lens[t], -inf up to max_context.  q_fp8 [T, H, 128]
     (float8_e4m3fn or uint8), weights [T, H] fp32, index_k_cache page-blocked
-    (page_size 64), block_table [T, n] int32, context_lens [T] int32.
+    (page_size 64), block_table [T, n >= ceil(max_context / 64)] int32 (the
+    binding asks the table to cover max_context, so that no read of it can
+    leave the tensor whatever the device-side context lengths are; contexts
+    longer than max_context are clamped to it), context_lens [T] int32.
     ``pdl``: False, True, or "early" (PDL plus FLAG_PDL_EARLY_INDEX: the
     block table and context lengths are not written by the previous kernel).
     Returns logits [T, max_context] fp32."""
@@ -373,21 +397,30 @@ def dsa_indexer_mqa_logits(q_fp8, weights, index_k_cache, page_size, block_table
             or q_fp8.shape[2] != HEAD_DIM:
         raise ValueError("q_fp8 must be a contiguous CUDA [T, H, 128] tensor")
     T, H = q_fp8.shape[0], q_fp8.shape[1]
-    _need(weights, "weights", torch.float32, 2)
-    _need(block_table, "block_table", torch.int32, 2)
-    _need(context_lens, "context_lens", torch.int32, 1)
+    dev = q_fp8.device
+    _need(weights, "weights", torch.float32, 2, dev)
+    _need(block_table, "block_table", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    if not isinstance(index_k_cache, torch.Tensor) or index_k_cache.device != dev:
+        raise ValueError(f"index_k_cache must be a tensor on {dev}")
     if not weights.is_contiguous() or tuple(weights.shape) != (T, H):
         raise ValueError("weights must be contiguous [T, H]")
+    if block_table.shape[0] < T or block_table.shape[1] * page_size < int(max_context):
+        # every table read stays inside the tensor: contexts are clamped to max_context
+        raise ValueError("block_table must be [T, >= ceil(max_context / page_size)]")
+    if context_lens.shape[0] < T:
+        raise ValueError(f"context_lens has fewer than {T} entries")
     if logits is None:
-        logits = torch.empty((T, max(int(max_context), 1)), dtype=torch.float32,
-                             device=q_fp8.device)
-    _need(logits, "logits", torch.float32, 2)
+        logits = torch.empty((T, max(int(max_context), 1)), dtype=torch.float32, device=dev)
+    _need(logits, "logits", torch.float32, 2, dev)
+    if logits.shape[0] < T:
+        raise ValueError(f"logits has fewer than {T} rows")
     st = library().dsa_indexer_mqa_logits(
         _ptr(q_fp8), _ptr(weights), _ptr(index_k_cache), _num_pages(index_k_cache, page_size),
         page_size, _ptr(block_table), block_table.stride(0), _ptr(context_lens), _ptr(logits),
         logits.stride(0), int(max_context), T, H,
-        (FLAG_PDL if pdl else 0) | (FLAG_PDL_EARLY_INDEX if pdl == "early" else 0), _ptr(err_flags),
-        _stream(stream))
+        (FLAG_PDL if pdl else 0) | (FLAG_PDL_EARLY_INDEX if pdl == "early" else 0), _err_ptr(err_flags, q_fp8.device),
+        _stream(stream, q_fp8.device))
     if st != 0:
         raise DsaError(st, "dsa_indexer_mqa_logits")
     return logits[:, :max_context]

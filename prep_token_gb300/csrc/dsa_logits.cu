@@ -221,6 +221,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
     }
   };
   auto tiles_of = [](int len) { return len > 0 ? (len + kTileKeys - 1) / kTileKeys : 0; };
+  // keys past max_context have no column: the context is clamped to it
+  auto context_of = [&](int t) { return max(0, min(__ldg(p.context_lens + t), p.max_context)); };
   int cur[2 * kBatch];
   int len = 0;
   if (p.early_index) {
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
     // not written by the previous kernel.  The producer also starts its first
     // pages on their way into L2 (a hint, coherent with any write the
     // previous kernel makes to them) while that kernel finishes.
-    len = __ldg(p.context_lens + t);
+    len = context_of(t);
     if (warp == 0 && lane == 0) {
       const int nt = tiles_of(len);
       load_batch(static_cast<int>(blockIdx.x), nt, len, cur);
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
   grid_dependency_wait();
   grid_launch_dependents();
 
-  if (!p.early_index) len = __ldg(p.context_lens + t);
+  if (!p.early_index) len = context_of(t);
   const int ntiles = tiles_of(len);
 
   if (warp == 0) {

@@ -33,7 +33,7 @@ def _tolerance(li, tokens):
     P = li.page_size
     tol = np.zeros((len(tokens), li.max_context))
     for r, t in enumerate(tokens):
-        n = li.context_lens[t]
+        n = min(int(li.context_lens[t]), li.max_context)
         pages = cache[li.block_table[t, :(n + P - 1) // P]]
         kc = pages[:, :P * 128].reshape(-1, 128)[:n]
         ks = np.ascontiguousarray(pages[:, P * 128:]).view(np.float32).reshape(-1)[:n]
@@ -88,6 +88,8 @@ def test_partial_tiles_and_empty_context():
     li = synth.make_logits(seed=7, T=4, H=64, context=129)
     li.context_lens = np.array([0, 1, 64, 129], np.int32)
     li.max_context = 200
+    # the binding wants a table that covers max_context (padding entries unused)
+    li.block_table = np.pad(li.block_table, ((0, 0), (0, 4 - li.block_table.shape[1])))
     _check(li)
 
 
@@ -139,3 +141,36 @@ def test_pdl_graph_matches_eager(pdl):
     assert np.array_equal(np.isneginf(got), np.isneginf(eager))
     fin = np.isfinite(eager)
     assert np.array_equal(got[fin], eager[fin])
+
+
+def test_context_longer_than_max_context_is_clamped():
+    """Columns exist only below max_context: a longer context is clamped to it
+    (no wait is left hanging, no error bit), as the oracle defines."""
+    li = synth.make_logits(seed=12, T=3, H=32, context=600)
+    li.context_lens = np.array([600, 130, 0], np.int32)
+    li.max_context = 256
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _run_gpu(li, err=err)
+    assert int(err.item()) == 0
+    ref = _oracle(li, [0, 1, 2])
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isneginf(got), ~fin)
+    assert np.all(np.abs(got[fin] - ref[fin]) <= _tolerance(li, [0, 1, 2])[fin] + 1e-30)
+
+
+def test_binding_rejects_tensors_on_the_wrong_device_or_short_tables():
+    import prep_token_gb300 as dp
+    li = synth.make_logits(seed=13, T=2, H=16, context=200)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    args = [d(li.q_fp8), d(li.weights), d(li.cache), li.page_size, d(li.block_table),
+            d(li.context_lens), li.max_context]
+    bad = list(args)
+    bad[1] = torch.from_numpy(np.ascontiguousarray(li.weights))  # weights on the host
+    with pytest.raises(ValueError):
+        dp.dsa_indexer_mqa_logits(*bad)
+    bad = list(args)
+    bad[4] = args[4][:, :1]  # one 64-key block cannot cover max_context = 200
+    with pytest.raises(ValueError):
+        dp.dsa_indexer_mqa_logits(*bad)
+    with pytest.raises(ValueError):
+        dp.dsa_indexer_mqa_logits(*args, err_flags=torch.zeros(1, dtype=torch.int32))

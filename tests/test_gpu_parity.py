@@ -311,3 +311,30 @@ def test_token_major_prefill_full_size():
     inp = synth.make_prefill()
     inp.token_major = True
     _check(inp, kernels=("pipeline",))
+
+
+def test_binding_rejects_host_outputs_and_error_words():
+    """A host tensor in an output or error-word slot would hand the kernel a
+    host pointer: the binding refuses it before any launch."""
+    import prep_token_gb300 as dp
+    inp = synth.make_decode(seed=15, T=4, H=4)
+    d = to_device(inp)
+    base = (d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
+            d["beta"], inp.eps, inp.softmax_scale, new_cache(inp), inp.page_size, inp.rope_dim,
+            inp.style)
+    kw = dict(max_position=inp.max_position)
+    with pytest.raises(ValueError):
+        dp.dsa_indexer_qk_prepare_store(
+            *base, q_fp8_out=torch.empty((4, 4, 128), dtype=torch.uint8), **kw)
+    with pytest.raises(ValueError):
+        dp.dsa_indexer_qk_prepare_store(
+            *base, weights_out=torch.empty((4, 4), dtype=torch.float32), **kw)
+    with pytest.raises(TypeError):
+        dp.dsa_indexer_qk_prepare_store(
+            *base, q_fp8_out=torch.empty((4, 4, 128), dtype=torch.float16, device="cuda"), **kw)
+    with pytest.raises(ValueError):
+        dp.dsa_indexer_qk_prepare_store(*base, err_flags=torch.zeros(1, dtype=torch.int32), **kw)
+    with pytest.raises(ValueError):
+        dp.dsa_indexer_k_prepare_store(
+            d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
+            inp.eps, new_cache(inp).cpu(), inp.page_size, inp.rope_dim, inp.style, **kw)
