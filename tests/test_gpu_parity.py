@@ -338,3 +338,32 @@ def test_binding_rejects_host_outputs_and_error_words():
         dp.dsa_indexer_k_prepare_store(
             d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
             inp.eps, new_cache(inp).cpu(), inp.page_size, inp.rope_dim, inp.style, **kw)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_padded_strides_on_both_kernels(kernel):
+    """q with padded head and token strides (the pipeline kernel then copies
+    row by row), and cos/sin read from the first rope_dim/2 columns of wider
+    tables (cs_stride > rope_dim / 2): the same bytes as contiguous inputs."""
+    inp = synth.make_decode(seed=130, T=300, H=24, style=synth.NEOX)
+    d = to_device(inp)
+    ref = run_qk(inp, d, kernel=kernel)
+    qpad = torch.zeros((300, 24, 136), dtype=torch.bfloat16, device="cuda")
+    qpad[:, :, :128] = d["q"]
+    wide = lambda t: torch.cat([t, torch.full_like(t, 7.0)], dim=1)
+    dp_ = dict(d)
+    dp_["q"] = qpad[:, :, :128]
+    dp_["cos"] = wide(d["cos"])[:, :32]
+    dp_["sin"] = wide(d["sin"])[:, :32]
+    assert dp_["q"].stride() == (24 * 136, 136, 1) and dp_["cos"].stride(0) == 64
+    got = run_qk(inp, dp_, kernel=kernel)
+    for key in ("q_fp8", "weights", "cache"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert_parity(inp, ref, run_oracle_qk(inp))
+
+
+@pytest.mark.parametrize("T,H", [(3, 1000), (2, 4096)])
+def test_many_heads(T, H):
+    """Many head chunks per token (the pipeline kernel splits H into chunks
+    of at most 64 heads)."""
+    _check(synth.make_decode(seed=131 + H, T=T, H=H, style=synth.GPTJ))
