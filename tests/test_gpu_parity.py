@@ -285,12 +285,12 @@ def test_head_stride_not_contiguous_uses_per_head_copies():
     per head; the bytes must not change."""
     b = synth.make_decode(seed=17, T=300, H=24, style=synth.NEOX)
     db = to_device(b)
-    ref = run_qk(b, db)
+    ref = run_qk(b, db, kernel="pipeline")
     qpad = torch.zeros((300, 24, 136), dtype=torch.bfloat16, device="cuda")
     qpad[:, :, :128] = db["q"]
     dc = dict(db)
     dc["q"] = qpad[:, :, :128]
-    got = run_qk(b, dc)
+    got = run_qk(b, dc, kernel="pipeline")
     for key in ("q_fp8", "weights", "cache"):
         assert np.array_equal(got[key], ref[key]), key
     assert_parity(b, got, run_oracle_qk(b))
