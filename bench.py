@@ -496,6 +496,14 @@ def run_ours(args, rank, world, local_rank):
             stress[name] = {"us_per_call": us, "calls": calls, "gb_per_s": gbs,
                             "hbm_frac": gbs / peaks["hbm_gbs"],
                             "tokens_per_s": sinp.T / (us * 1e-6)}
+        # the k-only call on the same 65,536 keys (660 algorithmic bytes per key)
+        kus, kcalls = _prefill_graph_us(torch, [(sinp, sd), (sinp, sd)], stream,
+                                        lambda inp, d: _call(dp, inp, d, stream, k_only=True),
+                                        min(args.steps, 200))
+        kbytes = sinp.T * 660 + 1024
+        stress["k_only"] = {"us_per_call": kus, "calls": kcalls,
+                            "gb_per_s": kbytes / (kus * 1e-6) / 1e9,
+                            "hbm_frac": kbytes / (kus * 1e-6) / 1e9 / peaks["hbm_gbs"]}
         del sd
 
     logits = None

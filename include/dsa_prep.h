@@ -104,8 +104,9 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
 /* Kernel choice.  By default calls with T * H <= 16384 query vectors take the
  * direct kernel (loads straight to registers: least latency, for decode) and
  * larger ones the pipeline kernel (bulk copies through a shared-memory ring:
- * most bandwidth, for prefill).  These flags force one; both give the same
- * bytes.  Setting both is an error. */
+ * most bandwidth, for prefill); the k-only call always takes the direct
+ * kernel.  These flags force one; both give the same bytes.  Setting both is
+ * an error. */
 #define DSA_FLAG_PIPELINE 2u
 #define DSA_FLAG_DIRECT 4u
 /* With DSA_FLAG_PDL only: the caller promises that positions, out_cache_loc

@@ -122,8 +122,11 @@ cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligne
   p.early_rope = (flags & DSA_FLAG_PDL_EARLY_ROPE) ? 1 : 0;
   p.test_withhold = (flags & DSA_FLAG_TEST_WITHHOLD_UNIT) ? 1 : 0;
   p.cg.token_major = (flags & DSA_FLAG_CACHE_TOKEN_MAJOR) ? 1 : 0;
-  const long long vecs = static_cast<long long>(p.T) * (p.H > 0 ? p.H : 1);
-  bool direct = vecs <= kDirectMaxVectors;
+  // The k-only call always takes the direct kernel: a pipeline unit would be
+  // one key, a single warp's work behind a barrier all eight consumers pass
+  // (3.7x slower at 65,536 keys).
+  const long long vecs = static_cast<long long>(p.T) * p.H;
+  bool direct = p.H == 0 || vecs <= kDirectMaxVectors;
   if (flags & DSA_FLAG_PIPELINE) direct = false;
   if (flags & DSA_FLAG_DIRECT) direct = true;
   if (direct) {
