@@ -230,8 +230,9 @@ __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params
   grid_launch_dependents();
   if (u >= p.q_warps + p.k_warps) return;  // warp-uniform
   // Under PDL what follows, up to the wait, runs while the previous kernel of
-  // the stream finishes.  The quarter-warp's input row starts on its way into
-  // L2 (a hint, safe whoever writes the row; see prefetch_l2_bulk).  With
+  // the stream finishes.  The quarter-warp's input row (and, for keys, the
+  // LayerNorm parameters) start on their way into L2 (a hint, safe whoever
+  // writes them; see prefetch_l2_bulk).  With
   // DSA_FLAG_PDL_EARLY_ROPE the caller guarantees that positions, slots and
   // the cos/sin cache are not written by the previous kernel, so their two
   // dependent round trips overlap its tail as well.
