@@ -93,11 +93,16 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def kernel_source_hash():
-    """sha256 over the sources the prefill kernel is compiled from."""
+def kernel_source_hash(files=None):
+    """sha256 over the sources a kernel is compiled from (the prefill kernel's
+    by default), with comments and whitespace removed, so that a comment edit
+    does not orphan the committed profile."""
     h = hashlib.sha256()
-    for f in KERNEL_SRCS:
-        h.update(open(f, "rb").read())
+    for f in files or KERNEL_SRCS:
+        src = open(f).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(re.sub(r"\s+", "", src).encode())
     return h.hexdigest()
 
 
