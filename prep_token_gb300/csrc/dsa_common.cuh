@@ -395,7 +395,9 @@ __device__ __forceinline__ float quad_sum(float v) {
 // ue8m0 exponent of the vector: the smallest e with max(amax, 1e-4) <= 448*2^e.
 // With A = max(amax, 1e-4) = 1.f * 2^E (normal), 448 * 2^e = 1.75 * 2^(e+8), so
 // e = E - 8 when the fraction is <= 0.75 (bits <= 0x600000) and E - 7 above:
-// read straight off the exponent and fraction bits, no division or log.
+// read straight off the exponent and fraction bits, no division or log.  The
+// compare rides a carry: fraction > 0x600000 exactly when fraction + 0x1fffff
+// reaches 2^23 and bumps the exponent field.
 __device__ __forceinline__ float vector_amax(const float (&x)[16]) {
   float m = max3f(fabsf(x[0]), fabsf(x[1]), fabsf(x[2]));
 #pragma unroll
@@ -406,7 +408,7 @@ __device__ __forceinline__ float vector_amax(const float (&x)[16]) {
 
 __device__ __forceinline__ int exponent_of_amax(float amax) {
   const uint32_t b = __float_as_uint(fmaxf(amax, 1e-4f));
-  return static_cast<int>(b >> 23) - 135 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0);
+  return static_cast<int>((b + 0x1fffffu) >> 23) - 135;
 }
 
 __device__ __forceinline__ int ue8m0_exponent(const float (&x)[16]) {
