@@ -149,3 +149,24 @@ def test_ue8m0_floor_and_range():
     assert oracle.ue8m0_exponent([3.3895314e38])[0] == 120
     assert oracle.ue8m0_exponent([448.0])[0] == 0
     assert oracle.ue8m0_exponent([np.nextafter(np.float32(448), np.float32(1e3))])[0] == 1
+
+
+def test_quantiser_is_scale_equivariant_and_odd():
+    """Scaling a vector by 2^k leaves its codes alone and moves its exponent by
+    k (while amax stays above the 1e-4 floor); negating it flips only the sign
+    bits.  An exponent off by one, a scale applied twice or a sign dropped in
+    the encoder breaks one of these."""
+    rng = np.random.default_rng(41)
+    for _ in range(200):
+        z = (rng.standard_t(3, 128) * rng.uniform(0.01, 100)).astype(np.float32)
+        codes, e = oracle.quantize_vector(z)
+        for k in (-7, -1, 1, 5):
+            zk = (z.astype(np.float64) * 2.0 ** k).astype(np.float32)
+            if np.max(np.abs(zk)) <= 1e-4:
+                continue
+            ck, ek = oracle.quantize_vector(zk)
+            assert ek == e + k and np.array_equal(ck, codes), k
+        cn, en = oracle.quantize_vector(-z)
+        assert en == e
+        nonzero = codes & 0x7F != 0
+        assert np.array_equal(cn[nonzero], codes[nonzero] ^ 0x80)

@@ -357,3 +357,23 @@ def test_worked_hadamard(worked):
     assert weights[0, 0] == np.float32(ex["expect_weight"])
     assert list(cache[:128]) == _expand(ex["expect_k_codes"])
     assert cache[64 * 128:64 * 128 + 4].view(np.float32)[0] == np.float32(2.0 ** -5)
+
+
+def test_token_order_does_not_matter():
+    """Each token is handled on its own: permuting the tokens (with their
+    positions, slots and weights) permutes the q codes and weights and leaves
+    the cache bytes as they were.  A token index mixed into another token's
+    row, position or slot breaks it."""
+    inp = synth.make_decode(seed=42, T=24, H=3)
+    ref = run_oracle_qk(inp)
+    perm = np.random.default_rng(43).permutation(inp.T)
+    p = synth.make_decode(seed=42, T=24, H=3)
+    p.q = np.ascontiguousarray(inp.q[perm])
+    p.kw = np.ascontiguousarray(inp.kw[perm])
+    p.k, p.w = p.kw[:, :128], p.kw[:, 128:128 + inp.H]
+    p.positions = np.ascontiguousarray(inp.positions[perm])
+    p.slots = np.ascontiguousarray(inp.slots[perm])
+    got = run_oracle_qk(p)
+    assert np.array_equal(got["q_fp8"], ref["q_fp8"][perm])
+    assert np.array_equal(got["weights"], ref["weights"][perm])
+    assert np.array_equal(got["cache"], ref["cache"])
