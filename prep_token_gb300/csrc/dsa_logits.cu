@@ -252,6 +252,12 @@ __global__ void __launch_bounds__(kLThreads, 1)
   grid_dependency_wait();
   grid_launch_dependents();
 
+  // The query tile does not depend on the context length: its copy goes out
+  // first, overlapping the length's read (every CTA waits for it before exit).
+  if (warp == 0 && lane == 0) {
+    mbar_arrive_expect_tx(qfull, L::kQBytes);
+    tma_load_2d(sbase + L::kOffQ, &tq, 0, t * NH, qfull);
+  }
   if (!p.early_index) len = context_of(t);
   const int ntiles = tiles_of(len);
 
@@ -260,10 +266,6 @@ __global__ void __launch_bounds__(kLThreads, 1)
     if (lane == 0) {
       int m = 0;
       bool ok = true;
-      if (ntiles > blockIdx.x) {
-        mbar_arrive_expect_tx(qfull, L::kQBytes);
-        tma_load_2d(sbase + L::kOffQ, &tq, 0, t * NH, qfull);
-      }
       int nxt[2 * kBatch];
       if (!p.early_index) load_batch(static_cast<int>(blockIdx.x), ntiles, len, cur);
       for (int i0 = blockIdx.x; ok && i0 < ntiles; i0 += kBatch * step) {
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
       volatile int never = 0;
       for (int d = (m > kKStages ? m - kKStages : 0); d < m; ++d)
         mbar_wait(full(d % kKStages), (d / kKStages) & 1, &never);
-      if (ntiles > blockIdx.x) mbar_wait(qfull, 0, &never);
+      mbar_wait(qfull, 0, &never);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
