@@ -95,6 +95,29 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// cp.async (LDGSTS): a thread copies 16 or 8 bytes from global to shared
+// memory without holding a register for them; completion is tracked per
+// thread in commit groups, so a later wait on an older group does not wait
+// for the copies of a newer one.  .cg streams through L2 only; .ca may also
+// keep the line in L1 (for data many warps read, such as gamma and beta).
+__device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16_ca(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's most recent groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Programmatic dependent launch: no-ops unless the launch carries the attribute.
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -233,6 +256,17 @@ __device__ __forceinline__ void load_f32_shared(uint32_t a, float* x) {
   load_words<SharedMem, 4 * N, ALIGN>(a, w);
 #pragma unroll
   for (int j = 0; j < N; ++j) x[j] = __uint_as_float(w[j]);
+}
+
+// N fp32 values at element offset `off` of an fp32 row held in global memory
+// (read-only cached) or in shared memory (byte address).
+template <int N, int ALIGN>
+__device__ __forceinline__ void load_f32_at(const float* row, int off, float* x) {
+  load_f32_global<N, ALIGN>(row + off, x);
+}
+template <int N, int ALIGN>
+__device__ __forceinline__ void load_f32_at(uint32_t row, int off, float* x) {
+  load_f32_shared<N, ALIGN>(row + 4 * off, x);
 }
 
 // Store `BYTES` bytes (packed little-endian in w[]) at global p when `pred`
@@ -378,6 +412,8 @@ __device__ __forceinline__ void rope_slice(float (&x)[16], const Rot<RP>& r) {
 }
 
 // Quarter-warp reductions (xor offsets 4, 2, 1 stay inside the 8-lane group).
+// (The single-instruction f32 max reduction over a lane mask measured slower
+// here than these three shuffles, in latency and in throughput.)
 __device__ __forceinline__ float quad_max(float v) {
   v = fmaxf(v, __shfl_xor_sync(kFull, v, 4));
   v = fmaxf(v, __shfl_xor_sync(kFull, v, 2));
@@ -390,6 +426,60 @@ __device__ __forceinline__ float quad_sum(float v) {
   v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 2));
   v = __fadd_rn(v, __shfl_xor_sync(kFull, v, 1));
   return v;
+}
+
+// LayerNorm statistics of the quarter-warp's 128-vector (16 values in each of
+// its 8 lanes): the mean and M2, the sum of squared deviations from it.  Each
+// lane takes the mean and M2 of its own 16 values (pairwise sums), then three
+// merges with the xor partners 4, 2 and 1 combine two sets a and b of n
+// values each as
+//   mean = (mean_a + mean_b) / 2,   M2 = M2_a + M2_b + d^2 * n / 2,
+// d = mean_b - mean_a (the pairwise update of Chan, Golub and LeVeque,
+// "Algorithms for computing the sample variance", 1983).  Every step is
+// symmetric in a and b, so the 8 lanes end with bit-identical results; three
+// shuffle rounds instead of the six of a two-pass sum.
+__device__ __forceinline__ void ln_stats(const float (&x)[16], float& mean, float& m2) {
+  float s[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(x[2 * j], x[2 * j + 1]);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) s[j] = __fadd_rn(s[2 * j], s[2 * j + 1]);
+  s[0] = __fadd_rn(s[0], s[1]);
+  s[1] = __fadd_rn(s[2], s[3]);
+  float m = __fmul_rn(__fadd_rn(s[0], s[1]), 1.0f / 16.0f);
+  float q[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float d0 = __fsub_rn(x[2 * j], m), d1 = __fsub_rn(x[2 * j + 1], m);
+    q[j] = __fmaf_rn(d1, d1, __fmul_rn(d0, d0));
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) q[j] = __fadd_rn(q[2 * j], q[2 * j + 1]);
+  q[0] = __fadd_rn(q[0], q[1]);
+  q[1] = __fadd_rn(q[2], q[3]);
+  float v = __fadd_rn(q[0], q[1]);
+  float half_n = 8.0f;  // n / 2, n = values per merged set
+#pragma unroll
+  for (int off = 4; off >= 1; off >>= 1) {
+    const float mo = __shfl_xor_sync(kFull, m, off);
+    const float vo = __shfl_xor_sync(kFull, v, off);
+    const float d = __fsub_rn(mo, m);
+    v = __fmaf_rn(d, __fmul_rn(d, half_n), __fadd_rn(v, vo));
+    m = __fmul_rn(__fadd_rn(m, mo), 0.5f);
+    half_n *= 2.0f;
+  }
+  mean = m;
+  m2 = v;
+}
+
+// rstd of the LayerNorm (biased variance, eps inside the root) from M2, and
+// x - mean in place.
+__device__ __forceinline__ float ln_center(float (&x)[16], float eps) {
+  float mean, m2;
+  ln_stats(x, mean, m2);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) x[j] = __fsub_rn(x[j], mean);
+  return __frsqrt_rn(__fadd_rn(__fmul_rn(m2, 1.0f / kD), eps));
 }
 
 // ue8m0 exponent of the vector: the smallest e with max(amax, 1e-4) <= 448*2^e.
@@ -773,20 +863,22 @@ __device__ __forceinline__ void store_index_k_h(const CacheGeom& g, long long sl
 
 // gamma and beta of the lane's 16 elements, in register order, loaded all at
 // once (for latency-bound callers: the loads overlap the LayerNorm sums).
-template <int STYLE, int RP>
-__device__ __forceinline__ void load_affine_slice(const float* gamma, const float* beta, int l,
-                                                  float (&g)[16], float (&b)[16]) {
+// The rows are fp32 [128] in global memory (const float*) or staged in shared
+// memory (a byte address).
+template <int STYLE, int RP, class A>
+__device__ __forceinline__ void load_affine_slice(A gamma, A beta, int l, float (&g)[16],
+                                                  float (&b)[16]) {
   using S = Slice<STYLE, RP>;
   if constexpr (RP > 0) {
     if constexpr (S::NEOX) {
-      load_f32_global<RP, S::ALIGN_A_F32>(gamma + RP * l, g);
-      load_f32_global<RP, S::ALIGN_A_F32>(beta + RP * l, b);
-      load_f32_global<RP, S::ALIGN_B_F32>(gamma + S::B_BASE + RP * l, g + RP);
-      load_f32_global<RP, S::ALIGN_B_F32>(beta + S::B_BASE + RP * l, b + RP);
+      load_f32_at<RP, S::ALIGN_A_F32>(gamma, RP * l, g);
+      load_f32_at<RP, S::ALIGN_A_F32>(beta, RP * l, b);
+      load_f32_at<RP, S::ALIGN_B_F32>(gamma, S::B_BASE + RP * l, g + RP);
+      load_f32_at<RP, S::ALIGN_B_F32>(beta, S::B_BASE + RP * l, b + RP);
     } else {
       float tg[2 * RP], tb[2 * RP];
-      load_f32_global<2 * RP, S::ALIGN_A_F32>(gamma + 2 * RP * l, tg);
-      load_f32_global<2 * RP, S::ALIGN_A_F32>(beta + 2 * RP * l, tb);
+      load_f32_at<2 * RP, S::ALIGN_A_F32>(gamma, 2 * RP * l, tg);
+      load_f32_at<2 * RP, S::ALIGN_A_F32>(beta, 2 * RP * l, tb);
 #pragma unroll
       for (int j = 0; j < RP; ++j) {
         g[j] = tg[2 * j], g[RP + j] = tg[2 * j + 1];
@@ -795,14 +887,14 @@ __device__ __forceinline__ void load_affine_slice(const float* gamma, const floa
     }
   }
   if constexpr (S::NP > 0) {
-    load_f32_global<S::NP, S::ALIGN_P_F32>(gamma + S::P_BASE + S::NP * l, g + 2 * RP);
-    load_f32_global<S::NP, S::ALIGN_P_F32>(beta + S::P_BASE + S::NP * l, b + 2 * RP);
+    load_f32_at<S::NP, S::ALIGN_P_F32>(gamma, S::P_BASE + S::NP * l, g + 2 * RP);
+    load_f32_at<S::NP, S::ALIGN_P_F32>(beta, S::P_BASE + S::NP * l, b + 2 * RP);
   }
 }
 
-template <int STYLE, int RP>
-__device__ __forceinline__ void load_affine_hslice(const float* gamma, const float* beta, int l,
-                                                   float (&g)[16], float (&b)[16]) {
+template <int STYLE, int RP, class A>
+__device__ __forceinline__ void load_affine_hslice(A gamma, A beta, int l, float (&g)[16],
+                                                   float (&b)[16]) {
   using S = HSlice<STYLE, RP>;
   constexpr int PIECE = S::W < 4 ? S::W : 4;
 #pragma unroll
@@ -811,8 +903,8 @@ __device__ __forceinline__ void load_affine_hslice(const float* gamma, const flo
     for (int i0 = 0; i0 < S::W; i0 += PIECE) {
       const int o = c * S::STRIDE + S::W * l + i0;
       float tg[PIECE], tb[PIECE];
-      load_f32_global<PIECE, 4 * PIECE>(gamma + o, tg);
-      load_f32_global<PIECE, 4 * PIECE>(beta + o, tb);
+      load_f32_at<PIECE, 4 * PIECE>(gamma, o, tg);
+      load_f32_at<PIECE, 4 * PIECE>(beta, o, tb);
 #pragma unroll
       for (int i = 0; i < PIECE; ++i) g[S::reg(c, i0 + i)] = tg[i], b[S::reg(c, i0 + i)] = tb[i];
     }

@@ -134,8 +134,14 @@ cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligne
     p.q_warps = static_cast<long long>(p.T) * p.NQ;
     p.k_warps = (static_cast<long long>(p.T) + 3) / 4;
     const long long warps = p.q_warps + p.k_warps;
-    cfg.gridDim = dim3(static_cast<unsigned>((warps + kDirectThreads / 32 - 1) / (kDirectThreads / 32)));
-    cfg.blockDim = dim3(kDirectThreads);
+    // Spread the warps over the SMs: as few per CTA as fill them once (a
+    // small call gets one warp per SM, so no two warps share an SM's issue
+    // slots), at most kDirectWarps.
+    long long wpc = (warps + sms - 1) / sms;
+    if (wpc < 1) wpc = 1;
+    if (wpc > kDirectWarps) wpc = kDirectWarps;
+    cfg.gridDim = dim3(static_cast<unsigned>((warps + wpc - 1) / wpc));
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * wpc));
     cfg.dynamicSmemBytes = 0;
     return cudaLaunchKernelEx(
         &cfg, (flags & DSA_FLAG_HADAMARD) ? kDirectHad[rope_style][ri] : kDirect[rope_style][ri], p);

@@ -31,7 +31,9 @@
 //     shared memory and store to HBM.  Bytes in flight are set by the ring
 //     (up to ~200 KB per SM), not by registers.
 //   * dsa_direct_kernel (small calls, decode): one warp per four vectors,
-//     loads straight to registers; the least latency per call.
+//     every input in flight at once in two cp.async groups (the position and
+//     slot first, so the cos/sin loads go out while the rows still travel),
+//     warps spread over the SMs; the least latency per call.
 // Both come in a Hadamard variant (HAD = true) that rotates every vector by
 // H_128 / sqrt(128) after RoPE; it uses the HSlice lane layout.
 // Every mbarrier wait is bounded in time (DSA_DEVERR_TIMEOUT); nothing traps.
@@ -127,33 +129,25 @@ __device__ __forceinline__ void raise_error(const Params& p, int bit) {
 
 // Key vector: LayerNorm (mean, biased variance, eps inside the root), RoPE
 // (then H_128 / sqrt(128) in the Hadamard variant), quantise, and store the
-// codes and the scale into slot `slot` of the cache.  EARLY_AFFINE loads all
-// of the lane's gamma and beta before the sums, so their latency overlaps
-// them (for the latency-bound decode kernel); otherwise they are loaded piece
-// by piece after the sums, which keeps fewer registers live.
-template <bool HAD, int STYLE, int RP, bool EARLY_AFFINE = false>
+// codes and the scale into slot `slot` of the cache.  STAGED_AFFINE reads
+// the lane's gamma and beta from shared memory (gamma at byte address
+// gb_smem, beta 512 bytes on), all before the sums (for the latency-bound
+// decode kernel, which stages them with its input row); otherwise they are
+// loaded from global memory piece by piece after the sums, which keeps fewer
+// registers live.
+template <bool HAD, int STYLE, int RP, bool STAGED_AFFINE = false>
 __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const Rot<RP>& r,
-                                        int l, bool real, bool pos_ok, long long slot) {
-  float ga[16], be[16];  // used only with EARLY_AFFINE
-  if constexpr (EARLY_AFFINE) {
+                                        int l, bool real, bool pos_ok, long long slot,
+                                        uint32_t gb_smem = 0) {
+  float ga[16], be[16];  // used only with STAGED_AFFINE
+  if constexpr (STAGED_AFFINE) {
     if constexpr (HAD)
-      load_affine_hslice<STYLE, RP>(p.gamma, p.beta, l, ga, be);
+      load_affine_hslice<STYLE, RP>(gb_smem, gb_smem + 4 * kD, l, ga, be);
     else
-      load_affine_slice<STYLE, RP>(p.gamma, p.beta, l, ga, be);
+      load_affine_slice<STYLE, RP>(gb_smem, gb_smem + 4 * kD, l, ga, be);
   }
-  float sum = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) sum = __fadd_rn(sum, x[j]);
-  const float mean = __fmul_rn(quad_sum(sum), 1.0f / kD);
-  float sq = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    x[j] = __fsub_rn(x[j], mean);
-    sq = __fmaf_rn(x[j], x[j], sq);
-  }
-  const float var = __fmul_rn(quad_sum(sq), 1.0f / kD);
-  const float rstd = __frsqrt_rn(__fadd_rn(var, p.eps));
-  if constexpr (EARLY_AFFINE)
+  const float rstd = ln_center(x, p.eps);
+  if constexpr (STAGED_AFFINE)
     apply_affine(x, rstd, ga, be);
   else if constexpr (HAD)
     affine_hslice<STYLE, RP>(p.gamma, p.beta, l, x, rstd);
@@ -189,6 +183,7 @@ __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const R
 // ================================================================ direct kernel
 
 constexpr int kDirectThreads = 256;
+constexpr int kDirectWarps = kDirectThreads / 32;
 
 // cos/sin of the lane's frequencies at row `row`, from global memory.
 template <int RP>
@@ -211,15 +206,34 @@ __device__ __forceinline__ bool token_rot(const Params& p, long long t, int l, l
   return pos_ok;
 }
 
+// Direct kernel: one warp per four vectors (a quarter-warp each) -- four
+// heads of one token, or four keys.  Key warps come first: the LayerNorm
+// makes theirs the longest chain.  Latency rules here, so every
+// input is in flight at once, in two cp.async groups per thread:
+//   group 1: the token's position (and the key's slot), 8 bytes each;
+//   group 2: the 256-byte input row (lane l copies bytes 16l and 128 + 16l)
+//            and, for key warps, gamma and beta (1 KB, the whole warp).
+// Waiting for group 1 alone, the quarter-warp reads the position and issues
+// the cos/sin loads while the rows are still on their way; then it waits for
+// group 2 and reads its slice from shared memory.
 template <bool HAD, int STYLE, int RP>
 __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params p) {
+  __shared__ __align__(16) unsigned char s_rows[kDirectWarps][4][2 * kD];
+  __shared__ __align__(16) float s_gb[kDirectWarps][2][kD];
+  __shared__ __align__(16) long long s_idx[kDirectWarps][4][2];
   const int lane = threadIdx.x & 31;
+  const int wi = threadIdx.x >> 5;
   const int qtr = lane >> 3;
   const int l = lane & 7;
-  const long long u = static_cast<long long>(blockIdx.x) * (kDirectThreads / 32) + (threadIdx.x >> 5);
-  const bool is_q = u < p.q_warps;
+  // Work items are numbered down the columns of the grid (warp wi of CTA b is
+  // item wi * gridDim + b), so the key warps, items 0 .. k_warps - 1, land on
+  // different SMs; the launcher sizes CTAs so that small calls get one warp
+  // per SM.
+  const long long u = static_cast<long long>(wi) * gridDim.x + blockIdx.x;
+  const bool is_q = u >= p.k_warps;
+  const long long uq = u - p.k_warps;
   // q warp: four heads of one token; k warp: four keys, one per quarter-warp
-  const long long t = is_q ? u / p.NQ : 4 * (u - p.q_warps) + qtr;
+  const long long t = is_q ? uq / p.NQ : 4 * u + qtr;
   const bool real = is_q || t < p.T;
   const long long tt = real ? t : 0;
   long long pos = 0;
@@ -229,50 +243,67 @@ __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params
   // this grid's completion on its own griddepcontrol.wait.
   grid_launch_dependents();
   if (u >= p.q_warps + p.k_warps) return;  // warp-uniform
+  const int v = is_q ? static_cast<int>(uq - t * p.NQ) * 4 + qtr : 0;
+  const bool valid = v < p.H;
+  // a quarter-warp past the last head re-reads head H-1 and stores nothing
+  const int vl = valid ? v : p.H - 1;
+  const unsigned char* row = reinterpret_cast<const unsigned char*>(
+      is_q ? p.q + t * p.sq_t + static_cast<long long>(vl) * p.sq_h : p.k + tt * p.sk_t);
   // Under PDL what follows, up to the wait, runs while the previous kernel of
   // the stream finishes.  The quarter-warp's input row (and, for keys, the
   // LayerNorm parameters) start on their way into L2 (a hint, safe whoever
-  // writes them; see prefetch_l2_bulk).  With
-  // DSA_FLAG_PDL_EARLY_ROPE the caller guarantees that positions, slots and
-  // the cos/sin cache are not written by the previous kernel, so their two
-  // dependent round trips overlap its tail as well.
+  // writes them; see prefetch_l2_bulk).  With DSA_FLAG_PDL_EARLY_ROPE the
+  // caller guarantees that positions, slots and the cos/sin cache are not
+  // written by the previous kernel, so their two dependent round trips
+  // overlap its tail as well.
   if (l == 0) {
+    prefetch_l2_bulk(row, 2 * kD);
     if (is_q) {
-      const int v = static_cast<int>(u - t * p.NQ) * 4 + qtr;
-      const int vl = v < p.H ? v : p.H - 1;
-      prefetch_l2_bulk(p.q + t * p.sq_t + vl * p.sq_h, 2 * kD);
       prefetch_l2(p.w + t * p.sw_t + vl);
-    } else {
-      prefetch_l2_bulk(p.k + tt * p.sk_t, 2 * kD);
-      if (qtr == 0) {
-        prefetch_l2_bulk(p.gamma, 4 * kD);
-        prefetch_l2_bulk(p.beta, 4 * kD);
-      }
+    } else if (qtr == 0) {
+      prefetch_l2_bulk(p.gamma, 4 * kD);
+      prefetch_l2_bulk(p.beta, 4 * kD);
     }
   }
   if (p.early_rope) pos_ok = token_rot<RP>(p, tt, l, pos, r);
   grid_dependency_wait();
 
+  const uint32_t s_idx_q = smem_u32(&s_idx[wi][qtr][0]);
+  if (l == 0) {
+    cp_async8(s_idx_q, p.pos + tt);
+    if (!is_q) cp_async8(s_idx_q + 8, p.loc + tt);
+  }
+  cp_async_commit();
+  const uint32_t s_row = smem_u32(&s_rows[wi][qtr][0]);
+  cp_async16_cg(s_row + 16 * l, row + 16 * l);
+  cp_async16_cg(s_row + 128 + 16 * l, row + 128 + 16 * l);
+  const uint32_t s_gbw = smem_u32(&s_gb[wi][0][0]);
+  if (!is_q) {
+    cp_async16_ca(s_gbw + 16 * lane, p.gamma + 4 * lane);
+    cp_async16_ca(s_gbw + 4 * kD + 16 * lane, p.beta + 4 * lane);
+  }
+  cp_async_commit();
+  const float wv =
+      is_q ? __uint_as_float(static_cast<uint32_t>(__ldg(p.w + t * p.sw_t + vl)) << 16) : 0.0f;
+  cp_async_wait<1>();
+  __syncwarp();
+  if (!p.early_rope) {
+    pos = s_idx[wi][qtr][0];
+    pos_ok = pos >= 0 && pos < p.max_pos;
+    load_rot_global<RP>(p, pos_ok ? pos : 0, l, r);
+  }
+  const long long slot = s_idx[wi][qtr][1];
+  cp_async_wait<0>();
+  __syncwarp();
+  float x[16];
+  load_vec<HAD, STYLE, RP, SharedMem>(s_row, l, x);
   if (is_q) {
-    const int v = static_cast<int>(u - t * p.NQ) * 4 + qtr;
-    const bool valid = v < p.H;
-    // a quarter-warp past the last head re-reads head H-1 and stores nothing
-    const int vl = valid ? v : p.H - 1;
-    float x[16];
-    load_vec<HAD, STYLE, RP, GlobalMem>(
-        reinterpret_cast<const unsigned char*>(p.q + t * p.sq_t + vl * p.sq_h), l, x);
-    const float wv = __uint_as_float(static_cast<uint32_t>(__ldg(p.w + t * p.sw_t + vl)) << 16);
-    if (!p.early_rope) pos_ok = token_rot<RP>(p, t, l, pos, r);
     const long long orow = t * p.H + v;
     const int e = q_slice<HAD, STYLE, RP>(x, r, p.q_out + orow * kD, l, valid && pos_ok);
     store_f32_cs(p.w_out + orow, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold),
                  valid && pos_ok && l == 0);
   } else {
-    float x[16];
-    load_vec<HAD, STYLE, RP, GlobalMem>(reinterpret_cast<const unsigned char*>(p.k + tt * p.sk_t), l, x);
-    const long long slot = __ldg(p.loc + tt);
-    if (!p.early_rope) pos_ok = token_rot<RP>(p, tt, l, pos, r);
-    k_slice<HAD, STYLE, RP, true>(p, x, r, l, real, pos_ok, slot);
+    k_slice<HAD, STYLE, RP, true>(p, x, r, l, real, pos_ok, slot, s_gbw);
   }
 }
 

@@ -116,6 +116,8 @@ __global__ void __launch_bounds__(kThreads) unfused_layernorm_kernel(const UPara
   float x[16] = {};
   if (real)
     load_slice<0, 0, GlobalMem>(reinterpret_cast<const unsigned char*>(p.k + t * p.sk_t), l, x);
+  // two-pass sums (the fused kernels merge per-lane statistics instead; the
+  // chain is a baseline, not a latency path)
   float sum = 0.0f;
 #pragma unroll
   for (int j = 0; j < 16; ++j) sum = __fadd_rn(sum, x[j]);
