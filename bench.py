@@ -31,6 +31,8 @@ kernel launch.  Prints ONE JSON line (rank 0):
              step, for the 4 -> 1 launch comparison
   stress     the heavy-tailed 65,536-token workload (1.7 GB per call) in
              both pairings: us/call and HBM GB/s
+  k_only     the k-only call (index-K store) on 65,536 heavy-tailed keys in
+             both pairings, cycling input sets larger than L2
   mqa_logits the indexer's fp8 paged MQA logits (the consumer of the index-K
              cache) on the tcgen05 tensor cores at the 16K-context decode step
   cpu_baseline  the oracle (plain C) on a bounded sample, one spawned process
@@ -329,6 +331,68 @@ def _decode_timings(dp, torch, dev, make, reps=30, layers=21, k_only_too=False,
     return out
 
 
+def _k_dev_inputs(inp, dev):
+    """Device buffers of a k-only call: the k|w rows, indices, rope table,
+    LayerNorm parameters and a zeroed index-K cache."""
+    import torch
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    kw = t(inp.kw.view(np.int16)).view(torch.bfloat16)
+    return dict(k=kw[:, :128], positions=t(inp.positions), slots=t(inp.slots), cos=t(inp.cos),
+                sin=t(inp.sin), gamma=t(inp.gamma), beta=t(inp.beta),
+                cache=torch.zeros(inp.cache_bytes, dtype=torch.uint8, device=dev))
+
+
+def _k_bulk_timing(dp, torch, dev, peaks, reps=20, n_sets=4):
+    """The k-only call at prefill size (65,536 keys, 8 sequences of 8192),
+    both pairings: us per call over a graph of 8 calls that cycles through
+    `n_sets` input sets (k|w rows, slots and caches; 4 x 43 MB, more than the
+    129 MB L2), so every call reads its keys from HBM."""
+    import synth
+    out = {}
+    for style, name in ((synth.NEOX, "neox"), (synth.GPTJ, "gptj")):
+        sets = []
+        for i in range(n_sets):
+            inp = synth.make_k_bulk(seed=6 + i, style=style)
+            sets.append((inp, _k_dev_inputs(inp, dev)))
+        stream = torch.cuda.Stream(device=dev)
+
+        def call(inp, d):
+            dp.dsa_indexer_k_prepare_store(
+                d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
+                inp.eps, d["cache"], inp.page_size, inp.rope_dim, inp.style,
+                max_position=inp.max_position, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for inp, d in sets:
+                call(inp, d)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(8):
+                call(*sets[i % n_sets])
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        del g
+        T = sets[0][0].T
+        us = e0.elapsed_time(e1) * 1000.0 / (8 * reps)
+        kbytes = synth.algorithmic_bytes(T, 0, with_q=False)
+        out[name] = {"us_per_call": us, "calls": 8 * reps, "gb_per_s": kbytes / (us * 1e-6) / 1e9,
+                     "hbm_frac": kbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+                     "keys_per_s": T / (us * 1e-6)}
+        out["workload"] = (f"k-only T={T} (8 x 8192 tokens) rope_dim=64, 2048 shuffled pages, "
+                           f"{n_sets} input sets cycled (larger than L2)")
+        out["algorithmic_bytes"] = kbytes
+        del sets
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import prep_token_gb300 as dp
@@ -501,15 +565,12 @@ def run_ours(args, rank, world, local_rank):
             stress[name] = {"us_per_call": us, "calls": calls, "gb_per_s": gbs,
                             "hbm_frac": gbs / peaks["hbm_gbs"],
                             "tokens_per_s": sinp.T / (us * 1e-6)}
-        # the k-only call on the same 65,536 keys (660 algorithmic bytes per key)
-        kus, kcalls = _prefill_graph_us(torch, [(sinp, sd), (sinp, sd)], stream,
-                                        lambda inp, d: _call(dp, inp, d, stream, k_only=True),
-                                        min(args.steps, 200))
-        kbytes = sinp.T * 660 + 1024
-        stress["k_only"] = {"us_per_call": kus, "calls": kcalls,
-                            "gb_per_s": kbytes / (kus * 1e-6) / 1e9,
-                            "hbm_frac": kbytes / (kus * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+        # the k-only call at the same size: its own section, on input sets larger than L2
         del sd
+
+    k_only = None
+    if not args.no_stress:
+        k_only = _k_bulk_timing(dp, torch, dev, peaks)
 
     logits = None
     if rank == 0 and not args.no_logits:
@@ -571,6 +632,7 @@ def run_ours(args, rank, world, local_rank):
         "hadamard": hadamard,
         "prefill_pdl": prefill_pdl,
         "stress": stress,
+        "k_only": k_only,
         "mqa_logits": logits,
         "cpu_baseline": cpu,
     }
@@ -834,6 +896,17 @@ def run_probe(which, local_rank):
         torch.cuda.synchronize(dev)
         print(f"probe logits: 6 calls (T={li.T}, H={li.H}, context={li.max_context})")
         return
+    if which == "k_only":
+        inp = synth.make_k_bulk()
+        d = _k_dev_inputs(inp, dev)
+        for _ in range(6):
+            dp.dsa_indexer_k_prepare_store(
+                d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
+                inp.eps, d["cache"], inp.page_size, inp.rope_dim, inp.style,
+                max_position=inp.max_position)
+        torch.cuda.synchronize(dev)
+        print(f"probe k_only: 6 calls (T={inp.T})")
+        return
     had = which.endswith("_hadamard")
     inp = synth.make_decode(seed=1) if which.startswith("decode") else synth.make_prefill(seed=3)
     d = _dev_inputs(inp, dev)
@@ -858,7 +931,7 @@ def main():
     ap.add_argument("--no-stress", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--probe", choices=("prefill", "decode", "logits", "prefill_hadamard",
-                                        "decode_hadamard"),
+                                        "decode_hadamard", "k_only"),
                     help="make 6 eager calls on that workload and exit (for profilers)")
     args = ap.parse_args()
     if args.warmup < 3:

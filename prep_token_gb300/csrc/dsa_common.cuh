@@ -98,8 +98,9 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 // cp.async (LDGSTS): a thread copies 16 or 8 bytes from global to shared
 // memory without holding a register for them; completion is tracked per
 // thread in commit groups, so a later wait on an older group does not wait
-// for the copies of a newer one.  .cg streams through L2 only; .ca may also
-// keep the line in L1 (for data many warps read, such as gamma and beta).
+// for the copies of a newer one.  .cg streams through L2 only (16 bytes);
+// .ca (4, 8 or 16 bytes) may also keep the line in L1, for data many warps
+// read, such as gamma and beta.
 __device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -108,6 +109,9 @@ __device__ __forceinline__ void cp_async16_ca(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -322,6 +326,11 @@ __device__ __forceinline__ void store_f32_cs(float* p, float v, bool pred) {
   DSA_ST_PRED("st.global.cs.f32 [%1], %2;", "r"(pred ? 1u : 0u), "l"(p), "f"(v));
 }
 
+// The same with the default cache policy.
+__device__ __forceinline__ void store_f32(float* p, float v, bool pred) {
+  DSA_ST_PRED("st.global.f32 [%1], %2;", "r"(pred ? 1u : 0u), "l"(p), "f"(v));
+}
+
 // ---------------------------------------------------------------- the slice
 
 // Where a lane's 16 elements live (element offsets inside the 128-vector and
@@ -430,34 +439,40 @@ __device__ __forceinline__ float quad_sum(float v) {
 
 // LayerNorm statistics of the quarter-warp's 128-vector (16 values in each of
 // its 8 lanes): the mean and M2, the sum of squared deviations from it.  Each
-// lane takes the mean and M2 of its own 16 values (pairwise sums), then three
-// merges with the xor partners 4, 2 and 1 combine two sets a and b of n
-// values each as
+// lane takes the mean and M2 of its own 16 values (pairwise sums, two at a
+// time in packed f32x2 instructions), then three merges with the xor
+// partners 4, 2 and 1 combine two sets a and b of n values each as
 //   mean = (mean_a + mean_b) / 2,   M2 = M2_a + M2_b + d^2 * n / 2,
 // d = mean_b - mean_a (the pairwise update of Chan, Golub and LeVeque,
 // "Algorithms for computing the sample variance", 1983).  Every step is
 // symmetric in a and b, so the 8 lanes end with bit-identical results; three
 // shuffle rounds instead of the six of a two-pass sum.
+__device__ __forceinline__ float2 f2(const float (&x)[16], int j) {
+  return make_float2(x[2 * j], x[2 * j + 1]);
+}
+
 __device__ __forceinline__ void ln_stats(const float (&x)[16], float& mean, float& m2) {
-  float s[8];
+  // sum: (x0 + x2 + ..., x1 + x3 + ...) as a tree of packed adds
+  float2 a[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(x[2 * j], x[2 * j + 1]);
+  for (int j = 0; j < 4; ++j) a[j] = __fadd2_rn(f2(x, 2 * j), f2(x, 2 * j + 1));
+  a[0] = __fadd2_rn(a[0], a[1]);
+  a[2] = __fadd2_rn(a[2], a[3]);
+  a[0] = __fadd2_rn(a[0], a[2]);
+  float m = __fmul_rn(__fadd_rn(a[0].x, a[0].y), 1.0f / 16.0f);
+  // M2 of the lane's values about its own mean
+  const float2 nm = make_float2(-m, -m);
+  float2 q[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) s[j] = __fadd_rn(s[2 * j], s[2 * j + 1]);
-  s[0] = __fadd_rn(s[0], s[1]);
-  s[1] = __fadd_rn(s[2], s[3]);
-  float m = __fmul_rn(__fadd_rn(s[0], s[1]), 1.0f / 16.0f);
-  float q[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float d0 = __fsub_rn(x[2 * j], m), d1 = __fsub_rn(x[2 * j + 1], m);
-    q[j] = __fmaf_rn(d1, d1, __fmul_rn(d0, d0));
+  for (int j = 0; j < 4; ++j) {
+    const float2 d0 = __fadd2_rn(f2(x, 2 * j), nm);
+    const float2 d1 = __fadd2_rn(f2(x, 2 * j + 1), nm);
+    q[j] = __ffma2_rn(d1, d1, __fmul2_rn(d0, d0));
   }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) q[j] = __fadd_rn(q[2 * j], q[2 * j + 1]);
-  q[0] = __fadd_rn(q[0], q[1]);
-  q[1] = __fadd_rn(q[2], q[3]);
-  float v = __fadd_rn(q[0], q[1]);
+  q[0] = __fadd2_rn(q[0], q[1]);
+  q[2] = __fadd2_rn(q[2], q[3]);
+  q[0] = __fadd2_rn(q[0], q[2]);
+  float v = __fadd_rn(q[0].x, q[0].y);
   float half_n = 8.0f;  // n / 2, n = values per merged set
 #pragma unroll
   for (int off = 4; off >= 1; off >>= 1) {
@@ -477,8 +492,13 @@ __device__ __forceinline__ void ln_stats(const float (&x)[16], float& mean, floa
 __device__ __forceinline__ float ln_center(float (&x)[16], float eps) {
   float mean, m2;
   ln_stats(x, mean, m2);
+  const float2 nm = make_float2(-mean, -mean);
 #pragma unroll
-  for (int j = 0; j < 16; ++j) x[j] = __fsub_rn(x[j], mean);
+  for (int j = 0; j < 8; ++j) {
+    const float2 d = __fadd2_rn(f2(x, j), nm);
+    x[2 * j] = d.x;
+    x[2 * j + 1] = d.y;
+  }
   return __frsqrt_rn(__fadd_rn(__fmul_rn(m2, 1.0f / kD), eps));
 }
 
@@ -579,71 +599,112 @@ struct CacheGeom {
   long long num_slots;
   long long page_bytes;  // page_size * 132
   int page_size;
+  int page_shift;  // log2(page_size) when it is a power of two, else -1
   int token_major;
 };
 
-template <int STYLE, int RP>
-__device__ __forceinline__ void store_index_k(const CacheGeom& g, long long slot, int l,
-                                              const uint32_t* wa, const uint32_t* wb,
-                                              const uint32_t* wp, int e) {
-  if (g.token_major) {
-    uint8_t* row = g.cache + slot * (kD + 4);
-    store_slice<STYLE, RP, 4>(row, l, wa, wb, wp);
-    if (l == 0) *reinterpret_cast<float*>(row + kD) = pow2f(e);
+// log2(page_size) for a power of two, else -1 (set by the host).
+inline int page_shift_of(int page_size) {
+  for (int s = 0; s < 31; ++s)
+    if ((1 << s) == page_size) return s;
+  return -1;
+}
+
+// (page, row in page) of a valid slot: a shift and a mask for a power-of-two
+// page size, else a 32-bit division while the slot fits (a 64-bit one is a
+// long instruction sequence).
+__device__ __forceinline__ void slot_page(const CacheGeom& g, long long slot, long long& page,
+                                          long long& off) {
+  if (g.page_shift >= 0) {
+    page = slot >> g.page_shift;
+    off = slot & (g.page_size - 1);
+  } else if (slot <= 0xffffffffLL) {
+    const uint32_t pg = static_cast<uint32_t>(slot) / static_cast<uint32_t>(g.page_size);
+    page = pg;
+    off = slot - static_cast<long long>(pg) * g.page_size;
   } else {
-    const long long page = slot / g.page_size;
-    const long long off = slot - page * g.page_size;
-    uint8_t* base = g.cache + page * g.page_bytes;
-    store_slice<STYLE, RP>(base + off * kD, l, wa, wb, wp);
-    if (l == 0)
-      *reinterpret_cast<float*>(base + static_cast<long long>(g.page_size) * kD + 4 * off) =
-          pow2f(e);
+    page = slot / g.page_size;
+    off = slot - page * g.page_size;
   }
 }
 
-// y = x * rstd * gamma + beta on n values whose gamma/beta start at `row`
-// (fp32 [128] rows), one aligned piece at a time to keep few registers live.
-template <int N, int ALIGN>
-__device__ __forceinline__ void affine_piece(const float* g_row, const float* b_row, float* x,
-                                             float rstd) {
+// Store one key's codes and scale into slot `slot` (a valid slot) when
+// `pred` holds; the predicate rides on the store instructions.
+template <int STYLE, int RP>
+__device__ __forceinline__ void store_index_k(const CacheGeom& g, long long slot, int l,
+                                              const uint32_t* wa, const uint32_t* wb,
+                                              const uint32_t* wp, int e, bool pred = true) {
+  if (g.token_major) {
+    uint8_t* row = g.cache + slot * (kD + 4);
+    store_slice<STYLE, RP, 4>(row, l, wa, wb, wp, pred);
+    store_f32(reinterpret_cast<float*>(row + kD), pow2f(e), pred && l == 0);
+  } else {
+    long long page, off;
+    slot_page(g, slot, page, off);
+    uint8_t* base = g.cache + page * g.page_bytes;
+    store_slice<STYLE, RP>(base + off * kD, l, wa, wb, wp, pred);
+    store_f32(reinterpret_cast<float*>(base + static_cast<long long>(g.page_size) * kD + 4 * off),
+              pow2f(e), pred && l == 0);
+  }
+}
+
+// y = x * rstd * gamma + beta on N values (at offset `at` of each of M
+// vectors) whose gamma/beta start at `row` (fp32 [128] rows), one aligned
+// piece at a time to keep few registers live; the piece is loaded once for
+// all M vectors.
+template <int N, int ALIGN, int M>
+__device__ __forceinline__ void affine_piece(const float* g_row, const float* b_row,
+                                             float (&x)[M][16], int at, const float (&rstd)[M]) {
   float g[N], b[N];
   load_f32_global<N, ALIGN>(g_row, g);
   load_f32_global<N, ALIGN>(b_row, b);
 #pragma unroll
-  for (int j = 0; j < N; ++j) x[j] = __fmaf_rn(__fmul_rn(x[j], rstd), g[j], b[j]);
+  for (int m = 0; m < M; ++m)
+#pragma unroll
+    for (int j = 0; j < N; ++j) x[m][at + j] = __fmaf_rn(__fmul_rn(x[m][at + j], rstd[m]), g[j], b[j]);
 }
 
-template <int STYLE, int RP>
+template <int STYLE, int RP, int M>
 __device__ __forceinline__ void affine_slice(const float* gamma, const float* beta, int l,
-                                             float (&x)[16], float rstd) {
+                                             float (&x)[M][16], const float (&rstd)[M]) {
   using S = Slice<STYLE, RP>;
   if constexpr (RP > 0) {
     if constexpr (S::NEOX) {
-      affine_piece<RP, S::ALIGN_A_F32>(gamma + RP * l, beta + RP * l, x, rstd);
+      affine_piece<RP, S::ALIGN_A_F32>(gamma + RP * l, beta + RP * l, x, 0, rstd);
       affine_piece<RP, S::ALIGN_B_F32>(gamma + S::B_BASE + RP * l, beta + S::B_BASE + RP * l,
-                                       x + RP, rstd);
+                                       x, RP, rstd);
     } else {
       float g[2 * RP], b[2 * RP];
       load_f32_global<2 * RP, S::ALIGN_A_F32>(gamma + 2 * RP * l, g);
       load_f32_global<2 * RP, S::ALIGN_A_F32>(beta + 2 * RP * l, b);
 #pragma unroll
-      for (int j = 0; j < RP; ++j) {
-        x[j] = __fmaf_rn(__fmul_rn(x[j], rstd), g[2 * j], b[2 * j]);
-        x[RP + j] = __fmaf_rn(__fmul_rn(x[RP + j], rstd), g[2 * j + 1], b[2 * j + 1]);
-      }
+      for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int j = 0; j < RP; ++j) {
+          x[m][j] = __fmaf_rn(__fmul_rn(x[m][j], rstd[m]), g[2 * j], b[2 * j]);
+          x[m][RP + j] = __fmaf_rn(__fmul_rn(x[m][RP + j], rstd[m]), g[2 * j + 1], b[2 * j + 1]);
+        }
     }
   }
   constexpr int NP = S::NP;
   if constexpr (NP > 0) {
-    // pieces of at most 4 values
-    constexpr int PIECE = NP >= 4 ? 4 : NP;
+    // pieces of 4, 2 or 1 values, whichever divides the chunk (14 values at
+    // rope_dim 16)
+    constexpr int PIECE = NP % 4 == 0 ? 4 : NP % 2 == 0 ? 2 : 1;
 #pragma unroll
     for (int j = 0; j < NP; j += PIECE) {
       constexpr int A = S::ALIGN_P_F32 < 4 * PIECE ? S::ALIGN_P_F32 : 4 * PIECE;
-      affine_piece<PIECE, A>(gamma + S::P_BASE + NP * l + j, beta + S::P_BASE + NP * l + j,
-                             x + 2 * RP + j, rstd);
+      affine_piece<PIECE, A>(gamma + S::P_BASE + NP * l + j, beta + S::P_BASE + NP * l + j, x,
+                             2 * RP + j, rstd);
     }
   }
+}
+
+template <int STYLE, int RP>
+__device__ __forceinline__ void affine_slice(const float* gamma, const float* beta, int l,
+                                             float (&x)[16], float rstd) {
+  const float r1[1] = {rstd};
+  affine_slice<STYLE, RP, 1>(gamma, beta, l, reinterpret_cast<float (&)[1][16]>(x), r1);
 }
 
 
@@ -710,9 +771,9 @@ __device__ __forceinline__ void load_hslice(typename M::Addr row, int l, float (
   }
 }
 
-template <int STYLE, int RP>
+template <int STYLE, int RP, int M>
 __device__ __forceinline__ void affine_hslice(const float* gamma, const float* beta, int l,
-                                              float (&x)[16], float rstd) {
+                                              float (&x)[M][16], const float (&rstd)[M]) {
   using S = HSlice<STYLE, RP>;
   constexpr int PIECE = S::W < 4 ? S::W : 4;
 #pragma unroll
@@ -724,11 +785,20 @@ __device__ __forceinline__ void affine_hslice(const float* gamma, const float* b
       load_f32_global<PIECE, 4 * PIECE>(gamma + o, g);
       load_f32_global<PIECE, 4 * PIECE>(beta + o, b);
 #pragma unroll
-      for (int i = 0; i < PIECE; ++i) {
-        float& v = x[S::reg(c, i0 + i)];
-        v = __fmaf_rn(__fmul_rn(v, rstd), g[i], b[i]);
-      }
+      for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int i = 0; i < PIECE; ++i) {
+          float& v = x[m][S::reg(c, i0 + i)];
+          v = __fmaf_rn(__fmul_rn(v, rstd[m]), g[i], b[i]);
+        }
     }
+}
+
+template <int STYLE, int RP>
+__device__ __forceinline__ void affine_hslice(const float* gamma, const float* beta, int l,
+                                              float (&x)[16], float rstd) {
+  const float r1[1] = {rstd};
+  affine_hslice<STYLE, RP, 1>(gamma, beta, l, reinterpret_cast<float (&)[1][16]>(x), r1);
 }
 
 // Butterflies on index bit log2(B) between two pairs of registers of the lane:
@@ -845,19 +915,18 @@ __device__ __forceinline__ void store_hslice(uint8_t* row, int l, const uint32_t
 
 template <int STYLE, int RP>
 __device__ __forceinline__ void store_index_k_h(const CacheGeom& g, long long slot, int l,
-                                                const uint32_t (&w)[4], int e) {
+                                                const uint32_t (&w)[4], int e, bool pred = true) {
   if (g.token_major) {
     uint8_t* row = g.cache + slot * (kD + 4);
-    store_hslice<STYLE, RP, 4>(row, l, w);
-    if (l == 0) *reinterpret_cast<float*>(row + kD) = pow2f(e);
+    store_hslice<STYLE, RP, 4>(row, l, w, pred);
+    store_f32(reinterpret_cast<float*>(row + kD), pow2f(e), pred && l == 0);
   } else {
-    const long long page = slot / g.page_size;
-    const long long off = slot - page * g.page_size;
+    long long page, off;
+    slot_page(g, slot, page, off);
     uint8_t* base = g.cache + page * g.page_bytes;
-    store_hslice<STYLE, RP>(base + off * kD, l, w);
-    if (l == 0)
-      *reinterpret_cast<float*>(base + static_cast<long long>(g.page_size) * kD + 4 * off) =
-          pow2f(e);
+    store_hslice<STYLE, RP>(base + off * kD, l, w, pred);
+    store_f32(reinterpret_cast<float*>(base + static_cast<long long>(g.page_size) * kD + 4 * off),
+              pow2f(e), pred && l == 0);
   }
 }
 
@@ -910,11 +979,17 @@ __device__ __forceinline__ void load_affine_hslice(A gamma, A beta, int l, float
     }
 }
 
-// y = x * rstd * gamma + beta with gamma and beta already in registers.
+// y = x * rstd * gamma + beta with gamma and beta already in registers, two
+// elements per packed instruction (each half rounds as the scalar form).
 __device__ __forceinline__ void apply_affine(float (&x)[16], float rstd, const float (&g)[16],
                                              const float (&b)[16]) {
+  const float2 r2 = make_float2(rstd, rstd);
 #pragma unroll
-  for (int j = 0; j < 16; ++j) x[j] = __fmaf_rn(__fmul_rn(x[j], rstd), g[j], b[j]);
+  for (int j = 0; j < 8; ++j) {
+    const float2 y = __ffma2_rn(__fmul2_rn(f2(x, j), r2), f2(g, j), f2(b, j));
+    x[2 * j] = y.x;
+    x[2 * j + 1] = y.y;
+  }
 }
 
 // bf16 of x, round to nearest even (two at a time): lo in the low half.

@@ -15,5 +15,10 @@ const KernelFn kDirectHad[2][5] = {
      direct_fn<true, 0, 4>(), direct_fn<true, 0, 8>()},
     {direct_fn<true, 1, 0>(), direct_fn<true, 1, 1>(), direct_fn<true, 1, 2>(),
      direct_fn<true, 1, 4>(), direct_fn<true, 1, 8>()}};
+const KernelFn kStreamHad[2][5] = {
+    {kstream_fn<true, 0, 0>(), kstream_fn<true, 0, 1>(), kstream_fn<true, 0, 2>(),
+     kstream_fn<true, 0, 4>(), kstream_fn<true, 0, 8>()},
+    {kstream_fn<true, 1, 0>(), kstream_fn<true, 1, 1>(), kstream_fn<true, 1, 2>(),
+     kstream_fn<true, 1, 4>(), kstream_fn<true, 1, 8>()}};
 
 }  // namespace dsa_prep_impl

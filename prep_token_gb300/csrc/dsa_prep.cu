@@ -43,6 +43,16 @@ const KernelFn kDirect[2][5] = {
     {direct_fn<false, 1, 0>(), direct_fn<false, 1, 1>(), direct_fn<false, 1, 2>(),
      direct_fn<false, 1, 4>(), direct_fn<false, 1, 8>()}};
 
+const KernelFn kStream[2][5] = {
+    {kstream_fn<false, 0, 0>(), kstream_fn<false, 0, 1>(), kstream_fn<false, 0, 2>(),
+     kstream_fn<false, 0, 4>(), kstream_fn<false, 0, 8>()},
+    {kstream_fn<false, 1, 0>(), kstream_fn<false, 1, 1>(), kstream_fn<false, 1, 2>(),
+     kstream_fn<false, 1, 4>(), kstream_fn<false, 1, 8>()}};
+
+// dynamic shared memory of the k-stream kernels, by rope_dim / 16 index
+const int kStreamSmem[5] = {kstream_smem<0>(), kstream_smem<1>(), kstream_smem<2>(),
+                            kstream_smem<4>(), kstream_smem<8>()};
+
 int max_pipeline_smem() { return kBarrierBytes + kStages * (kOffQ + kHCMax * 256); }
 
 // Per-device facts looked up once: the SM count, and whether the pipeline
@@ -66,12 +76,18 @@ cudaError_t device_info(int* sms) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     for (int s = 0; s < 2; ++s)
-      for (int r = 0; r < 5; ++r)
+      for (int r = 0; r < 5; ++r) {
         for (const KernelFn fn : {kPipeline[s][r], kPipelineHad[s][r]}) {
           e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    max_pipeline_smem());
           if (e != cudaSuccess) return e;
         }
+        for (const KernelFn fn : {kStream[s][r], kStreamHad[s][r]}) {
+          e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kStreamSmem[r]);
+          if (e != cudaSuccess) return e;
+        }
+      }
     d.ready = true;
   }
   *sms = d.sms;
@@ -80,6 +96,8 @@ cudaError_t device_info(int* sms) {
 
 // Calls up to this many query vectors (T * H) take the direct kernel.
 constexpr long long kDirectMaxVectors = 16384;
+// k-only calls with more keys than this take the k-stream kernel.
+constexpr long long kStreamMinKeys = 8192;
 
 // Pipeline units: whole tokens (HC = H, up to 64) when there are enough tokens
 // to fill the machine; otherwise heads are split (chunks of >= 8) until the
@@ -122,9 +140,23 @@ cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligne
   p.early_rope = (flags & DSA_FLAG_PDL_EARLY_ROPE) ? 1 : 0;
   p.test_withhold = (flags & DSA_FLAG_TEST_WITHHOLD_UNIT) ? 1 : 0;
   p.cg.token_major = (flags & DSA_FLAG_CACHE_TOKEN_MAJOR) ? 1 : 0;
-  // The k-only call always takes the direct kernel: a pipeline unit would be
-  // one key, a single warp's work behind a barrier all eight consumers pass
-  // (3.7x slower at 65,536 keys).
+  const bool had = (flags & DSA_FLAG_HADAMARD) != 0;
+  if (p.H == 0) {
+    // k-only: the direct kernel up to kStreamMinKeys keys (least latency),
+    // the k-stream kernel above (DSA_FLAG_PIPELINE forces it).
+    const bool stream_k =
+        !(flags & DSA_FLAG_DIRECT) && ((flags & DSA_FLAG_PIPELINE) || p.T > kStreamMinKeys);
+    if (stream_k) {
+      const long long steps = (static_cast<long long>(p.T) + kStreamKeys - 1) / kStreamKeys;
+      long long blocks = static_cast<long long>(sms) * kStreamCtas;
+      const long long need = (steps + kStreamWarps - 1) / kStreamWarps;
+      if (blocks > need) blocks = need;
+      cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+      cfg.blockDim = dim3(kStreamThreads);
+      cfg.dynamicSmemBytes = static_cast<size_t>(kStreamSmem[ri]);
+      return cudaLaunchKernelEx(&cfg, had ? kStreamHad[rope_style][ri] : kStream[rope_style][ri], p);
+    }
+  }
   const long long vecs = static_cast<long long>(p.T) * p.H;
   bool direct = p.H == 0 || vecs <= kDirectMaxVectors;
   if (flags & DSA_FLAG_PIPELINE) direct = false;
@@ -134,6 +166,8 @@ cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligne
     p.q_warps = static_cast<long long>(p.T) * p.NQ;
     p.k_warps = (static_cast<long long>(p.T) + 3) / 4;
     const long long warps = p.q_warps + p.k_warps;
+    // L2 hints before the PDL wait, in a launch of at most one wave
+    p.l2_hints = (flags & DSA_FLAG_PDL) && warps <= static_cast<long long>(sms) * kDirectWarps;
     // Spread the warps over the SMs: as few per CTA as fill them once (a
     // small call gets one warp per SM, so no two warps share an SM's issue
     // slots), at most kDirectWarps.
@@ -143,19 +177,17 @@ cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligne
     cfg.gridDim = dim3(static_cast<unsigned>((warps + wpc - 1) / wpc));
     cfg.blockDim = dim3(static_cast<unsigned>(32 * wpc));
     cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(
-        &cfg, (flags & DSA_FLAG_HADAMARD) ? kDirectHad[rope_style][ri] : kDirect[rope_style][ri], p);
+    return cudaLaunchKernelEx(&cfg, had ? kDirectHad[rope_style][ri] : kDirect[rope_style][ri], p);
   }
   choose_units(p, sms, w_rows_aligned);
   // one wave of persistent CTAs: as many as are resident at once
-  const int per_sm = (flags & DSA_FLAG_HADAMARD) ? kPipeCtasHad : kPipeCtas;
+  const int per_sm = had ? kPipeCtasHad : kPipeCtas;
   long long blocks = static_cast<long long>(sms) * per_sm;
   if (blocks > p.units) blocks = p.units;
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kPipeThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(kBarrierBytes + kStages * p.stage_bytes);
-  return cudaLaunchKernelEx(
-      &cfg, (flags & DSA_FLAG_HADAMARD) ? kPipelineHad[rope_style][ri] : kPipeline[rope_style][ri], p);
+  return cudaLaunchKernelEx(&cfg, had ? kPipelineHad[rope_style][ri] : kPipeline[rope_style][ri], p);
 }
 
 dsa_status check_k_side(const void* k, int64_t k_stride_t, const int64_t* positions,
@@ -217,6 +249,7 @@ void fill_k_side(Params& p, const void* k, int64_t k_stride_t, const int64_t* po
   p.cg.cache = static_cast<uint8_t*>(index_k_cache);
   p.cg.num_slots = num_pages * page_size;
   p.cg.page_size = page_size;
+  p.cg.page_shift = page_shift_of(page_size);
   p.cg.page_bytes = static_cast<long long>(page_size) * (kD + 4);
   p.T = T;
   p.rope_dim = rope_dim;
@@ -279,6 +312,7 @@ dsa_status dsa_indexer_k_prepare_store(
                                index_k_cache, num_pages, page_size, T, head_dim, rope_dim,
                                rope_style, flags);
   if (st != DSA_OK || T == 0) return st;
+  if (flags & DSA_FLAG_TEST_WITHHOLD_UNIT) return DSA_ERR_UNSUPPORTED;  // no producer warp here
   Params p = {};
   fill_k_side(p, k, k_stride_t, positions, out_cache_loc, cos_cache, sin_cache, cs_stride,
               max_position, ln_gamma, ln_beta, ln_eps, index_k_cache, num_pages, page_size, T,

@@ -87,6 +87,7 @@ struct Params {
   long long q_warps;  // warps doing q quads
   long long k_warps;  // warps doing keys (four per warp)
   int early_rope;     // read positions and cos/sin before the PDL wait
+  int l2_hints;       // prefetch the input rows into L2 before the PDL wait
   int test_withhold;  // DSA_FLAG_TEST_WITHHOLD_UNIT
   int* err;
 };
@@ -165,19 +166,59 @@ __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const R
     quantize_slice<STYLE, RP>(x, e, wa, wb, wp);
   }
 
-  if (!real) return;
-  if (!pos_ok) {
-    if (l == 0) raise_error(p, DSA_DEVERR_POSITION);
-    return;
-  }
-  if (slot < 0 || slot >= p.cg.num_slots) {
-    if (l == 0) raise_error(p, DSA_DEVERR_SLOT);
-    return;
-  }
+  // A key with a bad position or slot sets its error bit (the rare path)
+  // and stores nothing; the stores carry their predicate, not a branch.
+  const bool slot_ok = slot >= 0 && slot < p.cg.num_slots;
+  if (real && l == 0 && !(pos_ok && slot_ok))
+    raise_error(p, pos_ok ? DSA_DEVERR_SLOT : DSA_DEVERR_POSITION);
+  const bool store = real && pos_ok && slot_ok;
   if constexpr (HAD)
-    store_index_k_h<STYLE, RP>(p.cg, slot, l, wa, e);
+    store_index_k_h<STYLE, RP>(p.cg, store ? slot : 0, l, wa, e, store);
   else
-    store_index_k<STYLE, RP>(p.cg, slot, l, wa, wb, wp, e);
+    store_index_k<STYLE, RP>(p.cg, store ? slot : 0, l, wa, wb, wp, e, store);
+}
+
+// Several keys at once, N per quarter-warp: the steps of k_slice with gamma
+// and beta read piece by piece from global memory (k_slice<..., false>), each
+// phase run for all N keys before the next so their dependent chains
+// interleave, and each gamma/beta piece loaded once for all N.  Per key the
+// arithmetic is k_slice's, so the bytes written are the same.
+template <bool HAD, int STYLE, int RP, int N>
+__device__ __forceinline__ void k_multi(const Params& p, float (&x)[N][16], const Rot<RP> (&r)[N],
+                                        int l, const bool (&real)[N], const bool (&pos_ok)[N],
+                                        const long long (&slot)[N]) {
+  float rstd[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) rstd[n] = ln_center(x[n], p.eps);
+  if constexpr (HAD)
+    affine_hslice<STYLE, RP, N>(p.gamma, p.beta, l, x, rstd);
+  else
+    affine_slice<STYLE, RP, N>(p.gamma, p.beta, l, x, rstd);
+  int e[N];
+  uint32_t wa[N][4], wb[N][4], wp[N][4];
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    if constexpr (RP > 0) rope_slice<RP>(x[n], r[n]);
+    if constexpr (HAD) {
+      fwht_hslice<STYLE, RP>(x[n], l);
+      e[n] = hadamard_exponent(x[n]);
+      quantize_hslice<STYLE, RP>(x[n], e[n], wa[n]);
+    } else {
+      e[n] = ue8m0_exponent(x[n]);
+      quantize_slice<STYLE, RP>(x[n], e[n], wa[n], wb[n], wp[n]);
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    const bool slot_ok = slot[n] >= 0 && slot[n] < p.cg.num_slots;
+    if (real[n] && l == 0 && !(pos_ok[n] && slot_ok))
+      raise_error(p, pos_ok[n] ? DSA_DEVERR_SLOT : DSA_DEVERR_POSITION);
+    const bool store = real[n] && pos_ok[n] && slot_ok;
+    if constexpr (HAD)
+      store_index_k_h<STYLE, RP>(p.cg, store ? slot[n] : 0, l, wa[n], e[n], store);
+    else
+      store_index_k<STYLE, RP>(p.cg, store ? slot[n] : 0, l, wa[n], wb[n], wp[n], e[n], store);
+  }
 }
 
 // ================================================================ direct kernel
@@ -250,13 +291,15 @@ __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params
   const unsigned char* row = reinterpret_cast<const unsigned char*>(
       is_q ? p.q + t * p.sq_t + static_cast<long long>(vl) * p.sq_h : p.k + tt * p.sk_t);
   // Under PDL what follows, up to the wait, runs while the previous kernel of
-  // the stream finishes.  The quarter-warp's input row (and, for keys, the
-  // LayerNorm parameters) start on their way into L2 (a hint, safe whoever
-  // writes them; see prefetch_l2_bulk).  With DSA_FLAG_PDL_EARLY_ROPE the
+  // the stream finishes.  In a launch of one wave the quarter-warp's input
+  // row (and, for keys, the LayerNorm parameters) start on their way into L2
+  // (a hint, safe whoever writes them; see prefetch_l2_bulk).  The hints go
+  // through the bulk-copy engine, which takes small requests slowly, so a
+  // larger launch, or one without PDL, issues none.  With DSA_FLAG_PDL_EARLY_ROPE the
   // caller guarantees that positions, slots and the cos/sin cache are not
   // written by the previous kernel, so their two dependent round trips
   // overlap its tail as well.
-  if (l == 0) {
+  if (p.l2_hints && l == 0) {
     prefetch_l2_bulk(row, 2 * kD);
     if (is_q) {
       prefetch_l2(p.w + t * p.sw_t + vl);
@@ -304,6 +347,182 @@ __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params
                  valid && pos_ok && l == 0);
   } else {
     k_slice<HAD, STYLE, RP, true>(p, x, r, l, real, pos_ok, slot, s_gbw);
+  }
+}
+
+// ================================================================ k-stream kernel
+
+// Large k-only calls (the decode fast path's key store at prefill size):
+// persistent CTAs whose warps each own a contiguous range of keys, walked in
+// steps of kStreamKeys keys -- kStreamKPQ per quarter-warp, computed together
+// by k_multi.  Each lane holds the position and slot of one key of the warp's
+// current batch of 32 (and prefetches the next batch), so every input of a
+// step -- the key rows and their cos/sin row slices -- is copied by cp.async
+// into a stage of the warp's shared-memory ring kStreamStages - 1 steps ahead
+// of the math.  Per key the arithmetic is that of the other kernels, so every
+// kernel writes the same bytes.
+constexpr int kStreamKPQ = 2;                 // keys per quarter-warp per step
+constexpr int kStreamKeys = 4 * kStreamKPQ;   // keys per warp per step
+constexpr int kStreamWarps = 8;
+constexpr int kStreamThreads = 32 * kStreamWarps;
+constexpr int kStreamStages = 2;              // the step computed and the one in flight
+constexpr int kStreamCtas = 2;                // resident CTAs per SM the grid is sized for
+
+// Stage layout (bytes): kStreamKeys key rows ROW bytes apart, then the cos
+// and the sin slices of those keys (32 * RP bytes each: lane l's RP values at
+// 4 * RP * l), then per key its slot and whether its position is in range.
+// Key u of a step sits in quarter-warp u % 4.  ROW = 256 + 64 puts the rows of
+// quarter-warps 0 and 1 (and 2 and 3) in different banks, so an 8-byte slice
+// load of the whole warp takes two shared-memory wavefronts, not four.
+template <int RP>
+struct StreamStage {
+  static constexpr int ROW = 2 * kD + 64;
+  static constexpr int CS = 32 * RP;  // cos (or sin) bytes of one key
+  static constexpr int COS = kStreamKeys * ROW;
+  static constexpr int SIN = COS + kStreamKeys * CS;
+  static constexpr int IDX = SIN + kStreamKeys * CS;
+  static constexpr int BYTES = IDX + kStreamKeys * 16;
+};
+
+template <int RP>
+constexpr int kstream_smem() {
+  return kStreamWarps * kStreamStages * StreamStage<RP>::BYTES;
+}
+
+// cp.async of the lane's RP fp32 values (4 * RP bytes, aligned to that or 16).
+template <int RP>
+__device__ __forceinline__ void cp_async_rot(uint32_t dst, const float* src) {
+  if constexpr (RP == 8) {
+    cp_async16_ca(dst, src);
+    cp_async16_ca(dst + 16, src + 4);
+  } else if constexpr (RP == 4) {
+    cp_async16_ca(dst, src);
+  } else if constexpr (RP == 2) {
+    cp_async8(dst, src);
+  } else if constexpr (RP == 1) {
+    cp_async4(dst, src);
+  }
+}
+
+template <bool HAD, int STYLE, int RP>
+__global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kernel(const Params p) {
+  using SS = StreamStage<RP>;
+  constexpr int SPB = 32 / kStreamKeys;  // steps per batch of 32 keys
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31;
+  const int wi = threadIdx.x >> 5;
+  const int qtr = lane >> 3;
+  const int l = lane & 7;
+  // this warp's keys: [k0, k1), steps [w G / W, (w + 1) G / W) of the G
+  // steps, so the W warps' shares differ by one step at most
+  const long long nw = static_cast<long long>(gridDim.x) * kStreamWarps;
+  const long long steps = (static_cast<long long>(p.T) + kStreamKeys - 1) / kStreamKeys;
+  const long long w = static_cast<long long>(blockIdx.x) * kStreamWarps + wi;
+  const long long k0 = kStreamKeys * (w * steps / nw);
+  const long long k1 = min(static_cast<long long>(p.T), kStreamKeys * ((w + 1) * steps / nw));
+  const int n = k0 < k1 ? static_cast<int>((k1 - k0 + kStreamKeys - 1) / kStreamKeys) : 0;
+  grid_launch_dependents();
+  grid_dependency_wait();
+  const uint32_t ring = smem_u32(smem) + wi * kStreamStages * SS::BYTES;
+  unsigned char* ring_p = smem + wi * kStreamStages * SS::BYTES;
+
+  // position and slot of key k0 + 32 b + lane (clamped into the range)
+  auto batch = [&](int b, long long& pos, long long& slot) {
+    long long t = k0 + 32LL * b + lane;
+    t = t < k1 ? t : k1 - 1;
+    pos = __ldg(p.pos + t);
+    slot = __ldg(p.loc + t);
+  };
+  long long b_pos = 0, b_slot = 0, nb_pos = 0, nb_slot = 0;
+  if (n > 0) {  // the loads go out now; the first shuffle of b_pos waits for them
+    batch(0, b_pos, b_slot);
+    batch(1, nb_pos, nb_slot);
+  }
+  // Copy step j into its stage, as two cp.async groups (empty past the warp's
+  // last step).  Rows: for each of the step's keys u = 4h + q, lane l of
+  // quarter-warp q copies bytes 16l and 128 + 16l of the key row.  Rotation:
+  // each lane copies its own cos/sin values of the key, and lane 0 stores the
+  // key's slot and position check.  The rows need no position, so the first
+  // step's rows go out before the first batch of positions has arrived.
+  auto issue_rows = [&](int j) {
+    if (j < n) {
+      const uint32_t st = ring + (j % kStreamStages) * SS::BYTES;
+#pragma unroll
+      for (int h = 0; h < kStreamKPQ; ++h) {
+        const int u = 4 * h + qtr;
+        long long t = k0 + static_cast<long long>(kStreamKeys) * j + u;
+        t = t < k1 ? t : k1 - 1;
+        const unsigned char* row = reinterpret_cast<const unsigned char*>(p.k + t * p.sk_t);
+        cp_async16_cg(st + SS::ROW * u + 16 * l, row + 16 * l);
+        cp_async16_cg(st + SS::ROW * u + 128 + 16 * l, row + 128 + 16 * l);
+      }
+    }
+    cp_async_commit();
+  };
+  auto issue_rot = [&](int j) {
+    if (j < n) {
+      if (j > 0 && j % SPB == 0) {  // the next batch of 32 keys
+        b_pos = nb_pos;
+        b_slot = nb_slot;
+        batch(j / SPB + 1, nb_pos, nb_slot);
+      }
+      const uint32_t st = ring + (j % kStreamStages) * SS::BYTES;
+      unsigned char* st_p = ring_p + (j % kStreamStages) * SS::BYTES;
+#pragma unroll
+      for (int h = 0; h < kStreamKPQ; ++h) {
+        const int u = 4 * h + qtr;
+        const int src = kStreamKeys * (j % SPB) + u;
+        const long long pos = __shfl_sync(kFull, b_pos, src);
+        const long long slot = __shfl_sync(kFull, b_slot, src);
+        const bool pos_ok = pos >= 0 && pos < p.max_pos;
+        if constexpr (RP > 0) {
+          const long long crow = (pos_ok ? pos : 0) * p.cs_stride + RP * l;
+          cp_async_rot<RP>(st + SS::COS + SS::CS * u + 4 * RP * l, p.cos_t + crow);
+          cp_async_rot<RP>(st + SS::SIN + SS::CS * u + 4 * RP * l, p.sin_t + crow);
+        }
+        if (l == 0) {
+          long long* idx = reinterpret_cast<long long*>(st_p + SS::IDX + 16 * u);
+          idx[0] = slot;
+          idx[1] = pos_ok ? 1 : 0;
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+  // Groups in commit order: rows(0), rot(0), rows(1), rot(1), ...; with step
+  // j + 1 in flight, step j has landed once at most two groups are pending.
+  static_assert(kStreamStages == 2, "the wait counts below assume two stages");
+  issue_rows(0);
+  issue_rot(0);
+  for (int j = 0; j < n; ++j) {
+    // refill the stage freed by step j - 1, then wait for step j
+    issue_rows(j + 1);
+    issue_rot(j + 1);
+    cp_async_wait<2>();
+    __syncwarp();
+    const uint32_t st = ring + (j % kStreamStages) * SS::BYTES;
+    const unsigned char* st_p = ring_p + (j % kStreamStages) * SS::BYTES;
+    float x[kStreamKPQ][16];
+    Rot<RP> r[kStreamKPQ];
+    bool real[kStreamKPQ], pos_ok[kStreamKPQ];
+    long long slot[kStreamKPQ];
+#pragma unroll
+    for (int h = 0; h < kStreamKPQ; ++h) {
+      const int u = 4 * h + qtr;
+      const long long* idx = reinterpret_cast<const long long*>(st_p + SS::IDX + 16 * u);
+      slot[h] = idx[0];
+      pos_ok[h] = idx[1] != 0;
+      real[h] = k0 + static_cast<long long>(kStreamKeys) * j + u < k1;
+      load_vec<HAD, STYLE, RP, SharedMem>(st + SS::ROW * u, l, x[h]);
+      if constexpr (RP > 0) {
+        load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(st + SS::COS + SS::CS * u + 4 * RP * l, r[h].c);
+        load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(st + SS::SIN + SS::CS * u + 4 * RP * l, r[h].s);
+        finish_rot<RP>(r[h]);
+      }
+    }
+    k_multi<HAD, STYLE, RP, kStreamKPQ>(p, x, r, l, real, pos_ok, slot);
+    __syncwarp();  // every lane is done with this stage before it is refilled
   }
 }
 
@@ -540,10 +759,13 @@ template <bool HAD, int STYLE, int RP>
 constexpr KernelFn pipeline_fn() { return dsa_pipeline_kernel<HAD, STYLE, RP>; }
 template <bool HAD, int STYLE, int RP>
 constexpr KernelFn direct_fn() { return dsa_direct_kernel<HAD, STYLE, RP>; }
+template <bool HAD, int STYLE, int RP>
+constexpr KernelFn kstream_fn() { return dsa_kstream_kernel<HAD, STYLE, RP>; }
 
 // The Hadamard variant's kernels, [rope_style][rope_dim / 16 -> 0, 1, 2, 4, 8];
 // instantiated in their own translation unit.
 extern const KernelFn kPipelineHad[2][5];
 extern const KernelFn kDirectHad[2][5];
+extern const KernelFn kStreamHad[2][5];
 
 }  // namespace dsa_prep_impl

@@ -347,6 +347,7 @@ dsa_status dsa_indexer_qk_prepare_store_unfused(
   p.cg.num_slots = num_pages * page_size;
   p.cg.page_bytes = static_cast<long long>(page_size) * (kD + 4);
   p.cg.page_size = page_size;
+  p.cg.page_shift = page_shift_of(page_size);
   p.cg.token_major = (flags & DSA_FLAG_CACHE_TOKEN_MAJOR) ? 1 : 0;
   p.T = T;
   p.H = H;

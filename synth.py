@@ -310,6 +310,41 @@ def make_stress(seed=4, style=NEOX, n_seq=8, seq_len=8192, H=64, pages=2048):
     return inp
 
 
+def make_k_bulk(seed=6, style=NEOX, n_seq=8, seq_len=8192, H=64, pages=2048):
+    """The k-only call (the index-K store of the dense fast path) at prefill
+    size: the stress set's keys without the query side.  Keys ~ Student-t(3)
+    x 4 rounded to bf16, 1% of elements set to +-m * 2^j (m an E4M3 midpoint,
+    j in [-3, 0]), 1/1024 rows all zero (at least one); positions 0..seq_len-1
+    in each of n_seq sequences; slots through a shuffled page table.  k sits
+    in the fused [T, 128 + H] k|w projection layout (w ~ N(0,1)); q is empty."""
+    T = n_seq * seq_len
+    rng = np.random.default_rng(seed)
+    ss = np.random.SeedSequence(seed)
+    k32 = _student_t(ss.spawn(1)[0], T * D).reshape(T, D)
+    mids = e4m3_midpoints()
+    kmask = rng.random(k32.shape) < 0.01
+    nk = int(kmask.sum())
+    k32[kmask] = (np.where(rng.random(nk) < 0.5, -1.0, 1.0)
+                  * mids[rng.integers(0, 120, nk)].astype(np.float64)
+                  * np.exp2(rng.integers(-3, 1, nk))).astype(np.float32)
+    zk = np.flatnonzero(rng.random(T) < 1.0 / 1024)
+    k32[zk if zk.size else np.array([0])] = 0.0
+    w32 = _normal(ss.spawn(1)[0], T * H).reshape(T, H)
+    kw = np.zeros((T, (D + H + 7) // 8 * 8), np.uint16)
+    kw[:, :D] = to_bf16_bits(k32)
+    kw[:, D:D + H] = to_bf16_bits(w32)
+    positions = np.tile(np.arange(seq_len), n_seq).astype(np.int64)
+    perm = rng.permutation(pages)
+    seq = np.repeat(np.arange(n_seq), seq_len)
+    slots = (perm[seq * (seq_len // 64) + positions // 64] * 64 + positions % 64).astype(np.int64)
+    gamma, beta = _norm_params(rng)
+    cos, sin = rope_table(seq_len, 64)
+    return Inputs(name="k_bulk", T=T, H=H, rope_dim=64, style=style, page_size=64,
+                  num_pages=pages, max_position=seq_len, q=np.zeros((0, H, D), np.uint16),
+                  k=kw[:, :D], w=kw[:, D:D + H], positions=positions, slots=slots, cos=cos,
+                  sin=sin, gamma=gamma, beta=beta, kw=kw)
+
+
 CONFIGS = {
     "tiny": make_tiny,
     "decode": make_decode,

@@ -91,7 +91,7 @@ def test_rope_dims(rope_dim, style):
     _check(inp)
 
 
-@pytest.mark.parametrize("page_size", [4, 16, 64, 256])
+@pytest.mark.parametrize("page_size", [4, 12, 16, 64, 100, 256])
 def test_page_sizes(page_size):
     inp = synth.make_decode(seed=page_size, T=50, H=4)
     inp.page_size = page_size
