@@ -23,7 +23,9 @@ kernel launch.  Prints ONE JSON line (rank 0):
              indexer layers (shared positions / slots / rope cache, per-layer
              q, k|w, outputs and index-K cache) captured as a CUDA graph and
              replayed after an L2 flush -- plain, with PDL, and with PDL plus
-             early rope reads -- plus a single-call graph and eager calls
+             early rope reads -- plus a single-call graph, eager calls through
+             the binding, and eager calls through the C ABI with pre-bound
+             arguments (eager_abi_us, with their host time host_abi_us)
   hadamard   the Hadamard-rotated variant (q and k times H_128 / sqrt(128)
              after RoPE) on the prefill inputs and in the decode step
   unfused    the same call as four launches with bf16 intermediates (the
@@ -62,7 +64,14 @@ sys.path.insert(0, ROOT)
 
 METRIC = "tokens/s + achieved HBM GB/s (% of peak) prefill; µs/call at decode T=1..64"
 WORKLOAD = "prefill T=8192 H=64 D=128 rope_dim=64 NeoX, 128 pages x 64 (contiguous slots)"
-PROFILE = os.path.join(ROOT, "profiles", "dsa_pipeline_kernel_prefill_T8192_H64.md")
+# DRAM traffic of the kernels, per launch, from ncu (written by --traffic-from)
+TRAFFIC_JSON = {"prefill": os.path.join(ROOT, "profiles", "traffic_prefill_T8192_H64.json"),
+                "decode": os.path.join(ROOT, "profiles", "traffic_decode_T64_H64.json"),
+                "k_only": os.path.join(ROOT, "profiles", "traffic_k_only_T65536.json")}
+TRAFFIC_KERNEL = {"prefill": "dsa_pipeline_kernel", "decode": "dsa_direct_kernel",
+                  "k_only": "dsa_kstream_kernel"}
+TRAFFIC_METRICS = ("dram__bytes_read.sum,dram__bytes_write.sum,lts__t_sectors_op_write.sum,"
+                   "lts__t_sectors_op_read.sum,gpu__time_duration.sum")
 KERNEL_SRCS = [os.path.join(ROOT, "prep_token_gb300", "csrc", f)
                for f in ("dsa_prep.cu", "dsa_prep_kernels.cuh", "dsa_common.cuh")]
 L2_FLUSH_BYTES = 256 << 20
@@ -108,18 +117,59 @@ def kernel_source_hash(files=None):
     return h.hexdigest()
 
 
-def profile_traffic():
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source has changed since it was captured."""
-    if not os.path.exists(PROFILE):
+def profile_traffic(which="prefill"):
+    """DRAM bytes per launch (read + write) from the committed traffic summary
+    of that kernel, or None when its sources have changed since the capture."""
+    path = TRAFFIC_JSON[which]
+    if not os.path.exists(path):
         return None
-    text = open(PROFILE).read()
-    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
-    if not (m_b and m_h):
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_sha256") != kernel_source_hash():
         return None
-    cur = kernel_source_hash()
-    return float(m_b.group(1)) if cur == m_h.group(1) else None
+    return float(rec["dram_bytes_read_per_launch"] + rec["dram_bytes_write_per_launch"])
+
+
+def write_traffic_json(csv_path, which):
+    """Turn an ncu --csv launch list of the TRAFFIC_METRICS (two back-to-back
+    launches of one kernel, --cache-control none) into the committed summary:
+    the figures of the last launch, which also drains what the one before
+    left dirty in L2, so its DRAM writes are those of a launch in a stream."""
+    import csv
+    launches = {}
+    name = None
+    with open(csv_path) as f:
+        rows = list(csv.reader(f))
+    hdr = next(i for i, r in enumerate(rows) if r and r[0] == "ID")
+    cols = rows[hdr]
+    for r in rows[hdr + 1:]:
+        if len(r) != len(cols):
+            continue
+        d = dict(zip(cols, r))
+        name = d["Kernel Name"]
+        launches.setdefault(int(d["ID"]), {})[d["Metric Name"]] = float(d["Metric Value"].replace(",", ""))
+    last = launches[max(launches)]
+    probe = {"prefill": "prefill", "decode": "decode", "k_only": "k_only"}[which]
+    rec = {
+        "kernel": name,
+        "workload": {"prefill": "prefill T=8192 H=64 NeoX (synth.make_prefill(seed=3))",
+                     "decode": "decode T=64 H=64 GPT-J (synth.make_decode(seed=1))",
+                     "k_only": "k-only T=65536 (synth.make_k_bulk, four input sets cycled)"}[which],
+        "command": (f"ncu --metrics {TRAFFIC_METRICS} --cache-control none --clock-control none "
+                    f"-k regex:{TRAFFIC_KERNEL[which]} -s 2 -c 2 --csv --log-file traffic.csv "
+                    f"python bench.py --probe {probe}"),
+        "launches_captured": len(launches),
+        "dram_bytes_read_per_launch": last["dram__bytes_read.sum"],
+        "dram_bytes_write_per_launch": last["dram__bytes_write.sum"],
+        "lts_read_sector_bytes": last["lts__t_sectors_op_read.sum"] * 32,
+        "lts_write_sector_bytes": last["lts__t_sectors_op_write.sum"] * 32,
+        "duration_ns_under_ncu": last["gpu__time_duration.sum"],
+        "kernel_source_sha256": kernel_source_hash(),
+    }
+    with open(TRAFFIC_JSON[which], "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return rec
 
 
 class ClockSampler:
@@ -231,6 +281,21 @@ def _call(dp, inp, d, stream, T=None, k_only=False, pdl=False, unfused=False, ha
         max_position=inp.max_position, stream=stream, num_tokens=T, pdl=pdl, hadamard=hadamard)
 
 
+def _prepared(dp, inp, d, stream, k_only=False, hadamard=False):
+    """The decode call checked and bound once (dp.PreparedCall): each call is
+    then one ctypes call into the C ABI with pre-built arguments."""
+    if k_only:
+        return dp.prepare_k_prepare_store(
+            d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
+            inp.eps, d["cache"], inp.page_size, inp.rope_dim, inp.style,
+            max_position=inp.max_position, stream=stream, hadamard=hadamard)
+    return dp.prepare_qk_prepare_store(
+        d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
+        d["beta"], inp.eps, inp.softmax_scale, d["cache"], inp.page_size, inp.rope_dim,
+        inp.style, q_fp8_out=d["q_out"], weights_out=d["w_out"],
+        max_position=inp.max_position, stream=stream, hadamard=hadamard)
+
+
 def _prefill_graph_us(torch, sets, stream, call, steps):
     """us per call of `call(inp, d)` on the alternating prefill sets: a graph
     of 10 calls replayed up to 100 times (after 3 eager warm-up calls)."""
@@ -327,6 +392,27 @@ def _decode_timings(dp, torch, dev, make, reps=30, layers=21, k_only_too=False,
                 stream.synchronize()
                 times.append(e0.elapsed_time(e1) * 1000.0 / len(sets))
         res["eager_us"] = {"median": statistics.median(times), "best": min(times)}
+        if not unfused:
+            # eager through the C ABI with pre-bound arguments (no binding checks):
+            # device time per call and host time per call
+            calls = [_prepared(dp, inp, d, stream, k_only=k_only, hadamard=hadamard)
+                     for inp, d in sets]
+            times, host = [], []
+            with torch.cuda.stream(stream):
+                for _ in range(5):
+                    flush.fill_(1)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    h0 = time.perf_counter()
+                    for c in calls:
+                        c()
+                    host.append((time.perf_counter() - h0) * 1e6 / len(calls))
+                    e1.record(stream)
+                    stream.synchronize()
+                    times.append(e0.elapsed_time(e1) * 1000.0 / len(calls))
+            res["eager_abi_us"] = {"median": statistics.median(times), "best": min(times)}
+            res["host_abi_us"] = {"median": statistics.median(host), "best": min(host)}
         out[name] = res
     return out
 
@@ -897,15 +983,16 @@ def run_probe(which, local_rank):
         print(f"probe logits: 6 calls (T={li.T}, H={li.H}, context={li.max_context})")
         return
     if which == "k_only":
-        inp = synth.make_k_bulk()
-        d = _k_dev_inputs(inp, dev)
-        for _ in range(6):
+        sets = [synth.make_k_bulk(seed=6 + i) for i in range(4)]
+        sets = [(inp, _k_dev_inputs(inp, dev)) for inp in sets]
+        for i in range(6):  # cycling four sets (170 MB, more than L2), as the bench does
+            inp, d = sets[i % 4]
             dp.dsa_indexer_k_prepare_store(
                 d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
                 inp.eps, d["cache"], inp.page_size, inp.rope_dim, inp.style,
                 max_position=inp.max_position)
         torch.cuda.synchronize(dev)
-        print(f"probe k_only: 6 calls (T={inp.T})")
+        print(f"probe k_only: 6 calls (T={inp.T}, four input sets)")
         return
     had = which.endswith("_hadamard")
     inp = synth.make_decode(seed=1) if which.startswith("decode") else synth.make_prefill(seed=3)
@@ -933,6 +1020,9 @@ def main():
     ap.add_argument("--probe", choices=("prefill", "decode", "logits", "prefill_hadamard",
                                         "decode_hadamard", "k_only"),
                     help="make 6 eager calls on that workload and exit (for profilers)")
+    ap.add_argument("--traffic-from", nargs=2, metavar=("CSV", "WHICH"),
+                    help="write the traffic summary of WHICH (prefill | decode | k_only) "
+                         "from an ncu launch-list CSV of the traffic metrics, and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -940,6 +1030,9 @@ def main():
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)
     local_rank = _env_int("LOCAL_RANK", 0)
+    if args.traffic_from:
+        print(json.dumps(write_traffic_json(*args.traffic_from)))
+        return
     if args.probe:
         run_probe(args.probe, local_rank)
         return

@@ -31,6 +31,7 @@ __all__ = [
     "dsa_indexer_qk_prepare_store_unfused", "dsa_unfused_workspace_bytes",
     "dsa_indexer_qk_prepare_store_unfused_noalloc", "dsa_indexer_mqa_logits",
     "library", "cache_bytes", "cache_views",
+    "PreparedCall", "prepare_qk_prepare_store", "prepare_k_prepare_store",
 ]
 
 NEOX, GPTJ = 0, 1
@@ -348,13 +349,9 @@ def dsa_indexer_qk_prepare_store_unfused_noalloc(q, k, w, positions, out_cache_l
     return outs
 
 
-def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
-                                ln_beta, ln_eps, index_k_cache, page_size, rope_dim=64,
-                                rope_style=NEOX, *, err_flags=None, num_tokens=None,
-                                max_position=None, pdl=False, kernel="auto",
-                                cache_layout="paged", hadamard=False, stream=None):
-    """k-only prepare-and-store (one kernel launch); writes the cache in place.
-    ``hadamard=True`` rotates k by H_128 / sqrt(128) after RoPE."""
+def _k_args(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta, ln_eps,
+            index_k_cache, page_size, rope_dim, rope_style, num_tokens, max_position):
+    """Checks and the C argument list of the k-only call, up to rope_style."""
     cs_stride, rows = _k_common(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
                                 ln_beta, index_k_cache, rope_dim)
     T = k.shape[0] if num_tokens is None else int(num_tokens)
@@ -364,16 +361,86 @@ def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cach
         if t.shape[0] < T:
             raise ValueError(f"{name} has fewer than {T} rows")
     max_position = rows if max_position is None else int(max_position)
+    return (_ptr(k), k.stride(0), _ptr(positions), _ptr(out_cache_loc),
+            _ptr(cos_cache) if rope_dim else None, _ptr(sin_cache) if rope_dim else None,
+            cs_stride, max_position, _ptr(ln_gamma), _ptr(ln_beta), float(ln_eps),
+            _ptr(index_k_cache), _num_pages(index_k_cache, page_size), page_size, T, HEAD_DIM,
+            rope_dim, int(rope_style))
+
+
+def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
+                                ln_beta, ln_eps, index_k_cache, page_size, rope_dim=64,
+                                rope_style=NEOX, *, err_flags=None, num_tokens=None,
+                                max_position=None, pdl=False, kernel="auto",
+                                cache_layout="paged", hadamard=False, stream=None):
+    """k-only prepare-and-store (one kernel launch); writes the cache in place.
+    ``hadamard=True`` rotates k by H_128 / sqrt(128) after RoPE."""
+    args = _k_args(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta, ln_eps,
+                   index_k_cache, page_size, rope_dim, rope_style, num_tokens, max_position)
     st = library().dsa_indexer_k_prepare_store(
-        _ptr(k), k.stride(0), _ptr(positions), _ptr(out_cache_loc),
-        _ptr(cos_cache) if rope_dim else None, _ptr(sin_cache) if rope_dim else None,
-        cs_stride, max_position, _ptr(ln_gamma), _ptr(ln_beta), float(ln_eps),
-        _ptr(index_k_cache), _num_pages(index_k_cache, page_size), page_size, T, HEAD_DIM,
-        rope_dim, int(rope_style),
-        _flags(pdl, kernel) | _layout(cache_layout) | (FLAG_HADAMARD if hadamard else 0),
+        *args, _flags(pdl, kernel) | _layout(cache_layout) | (FLAG_HADAMARD if hadamard else 0),
         _err_ptr(err_flags, k.device), _stream(stream, k.device))
     if st != 0:
         raise DsaError(st, "dsa_indexer_k_prepare_store")
+
+
+class PreparedCall:
+    """One library call whose arguments were checked and converted once.
+
+    For callers with fixed buffers (static activation buffers, or the tensors
+    a CUDA graph was captured on): the checks of the plain binding cost about
+    ten microseconds of host time per call, while a prepared call is a single
+    ctypes call with pre-built arguments.  The tensors it was prepared on must
+    stay alive and in place, the stream is the one given (or current) at
+    preparation, and the call raises DsaError on a non-zero status.  Calling
+    it returns the outputs it writes (for the fused call: q_fp8, weights)."""
+
+    def __init__(self, fn, name, args, outs=None, keep=()):
+        self._fn = fn
+        self._name = name
+        self._args = tuple(t(a) if a is not None else None for t, a in zip(fn.argtypes, args))
+        self._outs = outs
+        self._keep = keep  # tensors whose pointers the arguments hold
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != 0:
+            raise DsaError(st, self._name)
+        return self._outs
+
+
+def prepare_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma,
+                             ln_beta, ln_eps, softmax_scale, index_k_cache, page_size,
+                             rope_dim=64, rope_style=NEOX, *, q_fp8_out=None, weights_out=None,
+                             err_flags=None, num_tokens=None, max_position=None, pdl=False,
+                             kernel="auto", cache_layout="paged", hadamard=False, stream=None):
+    """dsa_indexer_qk_prepare_store checked and bound once: returns a
+    PreparedCall that launches it on these buffers (see PreparedCall)."""
+    args, outs, _, _ = _qk_args(q, k, w, positions, out_cache_loc, cos_cache, sin_cache,
+                                ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
+                                page_size, rope_dim, rope_style, q_fp8_out, weights_out,
+                                num_tokens, max_position)
+    fn = library().dsa_indexer_qk_prepare_store
+    full = (*args, _flags(pdl, kernel) | _layout(cache_layout) | (FLAG_HADAMARD if hadamard else 0),
+            _err_ptr(err_flags, q.device), _stream(stream, q.device))
+    keep = (q, k, w, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta,
+            index_k_cache, err_flags) + tuple(outs)
+    return PreparedCall(fn, "dsa_indexer_qk_prepare_store", full, outs, keep)
+
+
+def prepare_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta,
+                            ln_eps, index_k_cache, page_size, rope_dim=64, rope_style=NEOX, *,
+                            err_flags=None, num_tokens=None, max_position=None, pdl=False,
+                            kernel="auto", cache_layout="paged", hadamard=False, stream=None):
+    """dsa_indexer_k_prepare_store checked and bound once (see PreparedCall)."""
+    args = _k_args(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta, ln_eps,
+                   index_k_cache, page_size, rope_dim, rope_style, num_tokens, max_position)
+    fn = library().dsa_indexer_k_prepare_store
+    full = (*args, _flags(pdl, kernel) | _layout(cache_layout) | (FLAG_HADAMARD if hadamard else 0),
+            _err_ptr(err_flags, k.device), _stream(stream, k.device))
+    keep = (k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta, index_k_cache,
+            err_flags)
+    return PreparedCall(fn, "dsa_indexer_k_prepare_store", full, None, keep)
 
 
 def dsa_indexer_mqa_logits(q_fp8, weights, index_k_cache, page_size, block_table, context_lens,

@@ -367,3 +367,37 @@ def test_many_heads(T, H):
     """Many head chunks per token (the pipeline kernel splits H into chunks
     of at most 64 heads)."""
     _check(synth.make_decode(seed=131 + H, T=T, H=H, style=synth.GPTJ))
+
+
+@pytest.mark.parametrize("kernel", ["direct", "pipeline"])
+def test_prepared_calls_match_binding(kernel):
+    """prepare_qk_prepare_store / prepare_k_prepare_store: checked and bound
+    once, called twice, they write exactly what the plain binding writes."""
+    import prep_token_gb300 as dp
+    inp = synth.make_decode(seed=91, T=48, H=16)
+    d = to_device(inp)
+    ref = run_qk(inp, d, kernel=kernel)
+    ref_k = run_k(inp, d, kernel=kernel)
+    cache = new_cache(inp)
+    q_out = torch.empty((inp.T, inp.H, 128), dtype=torch.float8_e4m3fn, device="cuda")
+    w_out = torch.empty((inp.T, inp.H), dtype=torch.float32, device="cuda")
+    call = dp.prepare_qk_prepare_store(
+        d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"],
+        d["beta"], inp.eps, inp.softmax_scale, cache, inp.page_size, inp.rope_dim, inp.style,
+        q_fp8_out=q_out, weights_out=w_out, max_position=inp.max_position, kernel=kernel)
+    for _ in range(2):
+        got_q, got_w = call()
+        torch.cuda.synchronize()
+        assert got_q.data_ptr() == q_out.data_ptr()
+        assert np.array_equal(got_q.view(torch.uint8).cpu().numpy(), ref["q_fp8"])
+        assert np.array_equal(got_w.cpu().numpy(), ref["weights"])
+        assert np.array_equal(cache.cpu().numpy(), ref["cache"])
+    cache_k = new_cache(inp)
+    kcall = dp.prepare_k_prepare_store(
+        d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"], inp.eps,
+        cache_k, inp.page_size, inp.rope_dim, inp.style, max_position=inp.max_position,
+        kernel=kernel)
+    for _ in range(2):
+        assert kcall() is None
+        torch.cuda.synchronize()
+        assert np.array_equal(cache_k.cpu().numpy(), ref_k["cache"])
