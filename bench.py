@@ -26,6 +26,7 @@ kernel launch.  Prints ONE JSON line (rank 0):
              early rope reads -- plus a single-call graph, eager calls through
              the binding, and eager calls through the C ABI with pre-bound
              arguments (eager_abi_us, with their host time host_abi_us)
+  prefill_few_heads  prefill (T = 8192) with H = 32 and H = 16 heads
   hadamard   the Hadamard-rotated variant (q and k times H_128 / sqrt(128)
              after RoPE) on the prefill inputs and in the decode step
   unfused    the same call as four launches with bf16 intermediates (the
@@ -619,6 +620,22 @@ def run_ours(args, rank, world, local_rank):
                    "gb_per_s": algo_bytes / (pdl_us * 1e-6) / 1e9,
                    "hbm_frac": algo_bytes / (pdl_us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
 
+    # prefill with fewer heads (units of 64 / H tokens): T = 8192, H = 32 and 16
+    few_heads = {}
+    for Hf in (32, 16):
+        fsets = []
+        for i in range(2):
+            finp = synth.make_prefill(seed=3 + Hf + 1000 * rank + i, H=Hf)
+            fsets.append((finp, _dev_inputs(finp, dev)))
+        fus, fcalls = _prefill_graph_us(
+            torch, fsets, stream, lambda inp, d: _call(dp, inp, d, stream), args.steps)
+        fbytes = synth.algorithmic_bytes(T, Hf)
+        fgb = fbytes / (fus * 1e-6) / 1e9
+        few_heads[f"prefill_T{T}_H{Hf}"] = {
+            "us_per_call": fus, "calls": fcalls, "gb_per_s": fgb, "hbm_frac": fgb / peaks["hbm_gbs"],
+            "tokens_per_s": T / (fus * 1e-6), "algorithmic_bytes": fbytes}
+        del fsets
+
     # the Hadamard-rotated variant: same bytes, more arithmetic per vector
     hadamard = None
     if not args.no_hadamard:
@@ -717,6 +734,7 @@ def run_ours(args, rank, world, local_rank):
         "unfused": unfused,
         "hadamard": hadamard,
         "prefill_pdl": prefill_pdl,
+        "prefill_few_heads": few_heads,
         "stress": stress,
         "k_only": k_only,
         "mqa_logits": logits,
@@ -995,7 +1013,12 @@ def run_probe(which, local_rank):
         print(f"probe k_only: 6 calls (T={inp.T}, four input sets)")
         return
     had = which.endswith("_hadamard")
-    inp = synth.make_decode(seed=1) if which.startswith("decode") else synth.make_prefill(seed=3)
+    if which.startswith("decode"):
+        inp = synth.make_decode(seed=1)
+    elif which.startswith("prefill_h"):
+        inp = synth.make_prefill(seed=3, H=int(which[len("prefill_h"):]))
+    else:
+        inp = synth.make_prefill(seed=3)
     d = _dev_inputs(inp, dev)
     stream = torch.cuda.current_stream()
     for _ in range(6):
@@ -1018,7 +1041,8 @@ def main():
     ap.add_argument("--no-stress", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--probe", choices=("prefill", "decode", "logits", "prefill_hadamard",
-                                        "decode_hadamard", "k_only"),
+                                        "decode_hadamard", "k_only", "prefill_h32",
+                                        "prefill_h16"),
                     help="make 6 eager calls on that workload and exit (for profilers)")
     ap.add_argument("--traffic-from", nargs=2, metavar=("CSV", "WHICH"),
                     help="write the traffic summary of WHICH (prefill | decode | k_only) "

@@ -10,6 +10,11 @@ const KernelFn kPipelineHad[2][5] = {
      pipeline_fn<true, 0, 4>(), pipeline_fn<true, 0, 8>()},
     {pipeline_fn<true, 1, 0>(), pipeline_fn<true, 1, 1>(), pipeline_fn<true, 1, 2>(),
      pipeline_fn<true, 1, 4>(), pipeline_fn<true, 1, 8>()}};
+const KernelFn kPipelineMultiHad[2][5] = {
+    {pipeline_fn<true, 0, 0, true>(), pipeline_fn<true, 0, 1, true>(), pipeline_fn<true, 0, 2, true>(),
+     pipeline_fn<true, 0, 4, true>(), pipeline_fn<true, 0, 8, true>()},
+    {pipeline_fn<true, 1, 0, true>(), pipeline_fn<true, 1, 1, true>(), pipeline_fn<true, 1, 2, true>(),
+     pipeline_fn<true, 1, 4, true>(), pipeline_fn<true, 1, 8, true>()}};
 const KernelFn kDirectHad[2][5] = {
     {direct_fn<true, 0, 0>(), direct_fn<true, 0, 1>(), direct_fn<true, 0, 2>(),
      direct_fn<true, 0, 4>(), direct_fn<true, 0, 8>()},

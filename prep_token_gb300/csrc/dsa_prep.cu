@@ -37,6 +37,11 @@ const KernelFn kPipeline[2][5] = {
      pipeline_fn<false, 0, 4>(), pipeline_fn<false, 0, 8>()},
     {pipeline_fn<false, 1, 0>(), pipeline_fn<false, 1, 1>(), pipeline_fn<false, 1, 2>(),
      pipeline_fn<false, 1, 4>(), pipeline_fn<false, 1, 8>()}};
+const KernelFn kPipelineMulti[2][5] = {
+    {pipeline_fn<false, 0, 0, true>(), pipeline_fn<false, 0, 1, true>(), pipeline_fn<false, 0, 2, true>(),
+     pipeline_fn<false, 0, 4, true>(), pipeline_fn<false, 0, 8, true>()},
+    {pipeline_fn<false, 1, 0, true>(), pipeline_fn<false, 1, 1, true>(), pipeline_fn<false, 1, 2, true>(),
+     pipeline_fn<false, 1, 4, true>(), pipeline_fn<false, 1, 8, true>()}};
 const KernelFn kDirect[2][5] = {
     {direct_fn<false, 0, 0>(), direct_fn<false, 0, 1>(), direct_fn<false, 0, 2>(),
      direct_fn<false, 0, 4>(), direct_fn<false, 0, 8>()},
@@ -53,19 +58,20 @@ const KernelFn kStream[2][5] = {
 const int kStreamSmem[5] = {kstream_smem<0>(), kstream_smem<1>(), kstream_smem<2>(),
                             kstream_smem<4>(), kstream_smem<8>()};
 
-int max_pipeline_smem() { return kBarrierBytes + kStages * (kOffQ + kHCMax * 256); }
+int max_pipeline_smem() { return kBarrierBytes + kStages * kMaxStageBytes; }
 
 // Per-device facts looked up once: the SM count, and whether the pipeline
 // kernels' dynamic shared-memory limit has been raised on that device.
 struct DeviceInfo {
   int sms = 0;
+  int smem_per_sm = 0;  // shared memory of one SM, bytes
   bool ready = false;
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-cudaError_t device_info(int* sms) {
+cudaError_t device_info(int* sms, int* smem_per_sm = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -75,9 +81,12 @@ cudaError_t device_info(int* sms) {
   if (!d.ready) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return e;
     for (int s = 0; s < 2; ++s)
       for (int r = 0; r < 5; ++r) {
-        for (const KernelFn fn : {kPipeline[s][r], kPipelineHad[s][r]}) {
+        for (const KernelFn fn : {kPipeline[s][r], kPipelineHad[s][r], kPipelineMulti[s][r],
+                                  kPipelineMultiHad[s][r]}) {
           e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    max_pipeline_smem());
           if (e != cudaSuccess) return e;
@@ -91,6 +100,7 @@ cudaError_t device_info(int* sms) {
     d.ready = true;
   }
   *sms = d.sms;
+  if (smem_per_sm) *smem_per_sm = d.smem_per_sm;
   return cudaSuccess;
 }
 
@@ -99,33 +109,64 @@ constexpr long long kDirectMaxVectors = 16384;
 // k-only calls with more keys than this take the k-stream kernel.
 constexpr long long kStreamMinKeys = 8192;
 
-// Pipeline units: whole tokens (HC = H, up to 64) when there are enough tokens
-// to fill the machine; otherwise heads are split (chunks of >= 8) until the
-// units cover the SMs.  Chunks hold a multiple of 8 heads when H >= 8, so each
-// chunk's weights start on a 16-byte boundary and can ride the bulk copies.
+// Pipeline units.  With few heads (H <= 32) and tokens enough to fill the
+// machine, a unit is 2 (H <= 32) or 4 (H <= 16) whole tokens, so a unit
+// still carries up to 64 query rows: one bulk copy when the rows are
+// contiguous, and all eight consumer warps busy (8 / TPU per token).  Otherwise a unit is one
+// token: all its heads (up to 64) when there are tokens enough, else heads
+// split into chunks of >= 8 until the units cover the SMs.  Chunks hold a
+// multiple of 8 heads when H >= 8, so each chunk's weights start on a 16-byte
+// boundary and can ride the bulk copies.
 void choose_units(Params& p, int sms, bool w_rows_aligned) {
+  p.TPU = 1;
   if (p.H == 0) {
     p.HC = 0;
     p.NC = 1;
   } else {
-    int nc = (p.H + kHCMax - 1) / kHCMax;
-    const long long target = 3LL * sms;
-    while (static_cast<long long>(p.T) * nc * 2 <= target && (p.H + 2 * nc - 1) / (2 * nc) >= 8)
-      nc *= 2;
-    int hc = (p.H + nc - 1) / nc;
-    if (hc > 8) hc = (hc + 7) / 8 * 8;
-    p.HC = hc;
-    p.NC = (p.H + hc - 1) / hc;
+    if (p.H <= 32) {
+      const int tpu = p.H <= 16 ? 4 : 2;  // 64 / H tokens, rounded down to 1, 2 or 4
+      if (static_cast<long long>(p.T) >= static_cast<long long>(tpu) * 2 * kPipeCtas * sms) p.TPU = tpu;
+    }
+    if (p.TPU > 1) {
+      p.HC = p.H;
+      p.NC = 1;
+    } else {
+      int nc = (p.H + kHCMax - 1) / kHCMax;
+      const long long target = 3LL * sms;
+      while (static_cast<long long>(p.T) * nc * 2 <= target && (p.H + 2 * nc - 1) / (2 * nc) >= 8)
+        nc *= 2;
+      int hc = (p.H + nc - 1) / nc;
+      if (hc > 8) hc = (hc + 7) / 8 * 8;
+      p.HC = hc;
+      p.NC = (p.H + hc - 1) / hc;
+    }
   }
-  p.units = static_cast<long long>(p.T) * p.NC;
-  p.stage_bytes = kOffQ + p.HC * 256;
+  p.tpu_shift = p.TPU == 4 ? 2 : p.TPU == 2 ? 1 : 0;
+  p.units = (static_cast<long long>(p.T) + p.TPU - 1) / p.TPU * p.NC;
   p.w_bulk = (w_rows_aligned && p.H % 8 == 0 && p.HC % 8 == 0) ? 1 : 0;
+  // stage layout: headers (32 B a token), key rows, cos rows, sin rows,
+  // weights, query rows (from a 128-byte boundary); one-token units keep
+  // the fixed layout kOff*
+  if (p.TPU == 1) {  // the fixed layout of one-token units
+    p.off_k = kOffK;
+    p.off_cos = kOffCos;
+    p.off_sin = kOffSin;
+    p.off_w = kOffW;
+    p.off_q = kOffQ;
+  } else {
+    p.off_k = 32 * p.TPU;
+    p.off_cos = p.off_k + 256 * p.TPU;
+    p.off_sin = p.off_cos + p.cs_bytes * p.TPU;
+    p.off_w = p.off_sin + p.cs_bytes * p.TPU;
+    p.off_q = (p.off_w + 2 * p.HC * p.TPU + 127) / 128 * 128;
+  }
+  p.stage_bytes = p.off_q + 256 * p.HC * p.TPU;
 }
 
 cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligned,
                    cudaStream_t stream) {
-  int sms = 0;
-  cudaError_t e = device_info(&sms);
+  int sms = 0, smem_per_sm = 0;
+  cudaError_t e = device_info(&sms, &smem_per_sm);
   if (e != cudaSuccess) return e;
   const int ri = rp_index(p.rope_dim);
   cudaLaunchConfig_t cfg = {};
@@ -180,14 +221,19 @@ cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligne
     return cudaLaunchKernelEx(&cfg, had ? kDirectHad[rope_style][ri] : kDirect[rope_style][ri], p);
   }
   choose_units(p, sms, w_rows_aligned);
-  // one wave of persistent CTAs: as many as are resident at once
-  const int per_sm = had ? kPipeCtasHad : kPipeCtas;
+  // one wave of persistent CTAs: as many as are resident at once (the
+  // kernel's register budget, or fewer if the ring's shared memory says so)
+  const int smem = kBarrierBytes + kStages * p.stage_bytes;
+  int per_sm = had ? kPipeCtasHad : kPipeCtas;
+  while (per_sm > 1 && per_sm * (smem + 1024) > smem_per_sm) --per_sm;
   long long blocks = static_cast<long long>(sms) * per_sm;
   if (blocks > p.units) blocks = p.units;
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kPipeThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(kBarrierBytes + kStages * p.stage_bytes);
-  return cudaLaunchKernelEx(&cfg, had ? kPipelineHad[rope_style][ri] : kPipeline[rope_style][ri], p);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  const KernelFn fn = p.TPU > 1 ? (had ? kPipelineMultiHad : kPipelineMulti)[rope_style][ri]
+                                 : (had ? kPipelineHad : kPipeline)[rope_style][ri];
+  return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 dsa_status check_k_side(const void* k, int64_t k_stride_t, const int64_t* positions,

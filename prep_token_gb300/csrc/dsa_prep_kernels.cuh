@@ -79,9 +79,14 @@ struct Params {
   // pipeline kernel
   int HC;         // heads per unit
   int NC;         // units per token
+  int TPU;        // tokens per unit: 1, 2 or 4 (more than 1 only when NC is 1)
+  int tpu_shift;  // log2(TPU)
   long long units;
   int stage_bytes;
   int w_bulk;     // the chunk's weights can be bulk-copied (16-byte aligned)
+  // stage layout (byte offsets): per-token headers at 0, then key rows,
+  // cos rows, sin rows, gate weights, query rows
+  int off_k, off_cos, off_sin, off_w, off_q;
   // direct kernel
   int NQ;            // quads of heads per token
   long long q_warps;  // warps doing q quads
@@ -529,6 +534,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
 // ================================================================ pipeline kernel
 
 constexpr int kHCMax = 64;        // heads per unit at most
+constexpr int kTPUMax = 4;        // tokens per unit at most
 constexpr int kStages = 4;        // shared-memory ring depth
 constexpr int kConsumers = 8;     // consumer warps per CTA
 constexpr int kPipeThreads = 32 * (1 + kConsumers);
@@ -536,26 +542,29 @@ constexpr int kPipeThreads = 32 * (1 + kConsumers);
 // thread <= 65536 / (kPipeThreads * this)); the launcher sizes grids to match.
 constexpr int kPipeCtas = 3;
 constexpr int kPipeCtasHad = 3;
-
-// stage layout (byte offsets from the stage base)
-constexpr int kOffHdr = 0;     // StageHeader
-constexpr int kOffK = 64;      // key row, 256 B
+constexpr int kBarrierBytes = 128;  // full[kStages], empty[kStages], abort flag
+// stage layout of one-token units (byte offsets from the stage base)
+constexpr int kOffK = 64;      // key row, 256 B (after the StageHeader)
 constexpr int kOffCos = 320;   // cos row, rope_dim/2 floats (<= 256 B)
 constexpr int kOffSin = 576;   // sin row
 constexpr int kOffW = 832;     // gate weights of the chunk, HC bf16 (<= 128 B)
 constexpr int kOffQ = 1024;    // HC query rows of 256 B
-constexpr int kBarrierBytes = 128;  // full[kStages], empty[kStages], abort flag
+// the largest stage: headers, key rows, cos and sin rows (<= 256 B each) and
+// weights of kTPUMax tokens, then query rows of at most kHCMax heads in all
+constexpr int kMaxStageBytes = 32 * kTPUMax + 256 * kTPUMax + 2 * 256 * kTPUMax + 128 + 256 * kHCMax;
 
+// Per-token header of a stage.
 struct StageHeader {
   long long pos;
   long long slot;
   int pos_ok;
+  int pad[3];
 };
 
-// Producer warp: lane 0 fills the ring; all lanes prefetch (position, slot)
-// for the next 32 units of this CTA.  The position-independent copies (query
+// Producer warp for units of one token (the layout kOff*): lane 0 fills the
+// ring; all lanes prefetch (position, slot) for the next 32 units of this CTA.  The position-independent copies (query
 // rows, key row, weights) go out before the position is known.
-static __device__ void producer(const Params& p, unsigned char* ring, uint32_t full0, uint32_t empty0,
+static __device__ void producer_single(const Params& p, unsigned char* ring, uint32_t full0, uint32_t empty0,
                          volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
   long long my_pos = 0, my_slot = 0;
@@ -624,7 +633,7 @@ static __device__ void producer(const Params& p, unsigned char* ring, uint32_t f
     if (lane == 0 && !withhold) {
       const bool pos_ok = pos >= 0 && pos < p.max_pos;
       const long long row = pos_ok ? pos : 0;
-      StageHeader* hd = reinterpret_cast<StageHeader*>(st + kOffHdr);
+      StageHeader* hd = reinterpret_cast<StageHeader*>(st);
       hd->pos = pos;
       hd->slot = slot;
       hd->pos_ok = pos_ok ? 1 : 0;
@@ -647,8 +656,146 @@ static __device__ void producer(const Params& p, unsigned char* ring, uint32_t f
   }
 }
 
+// Producer warp for units of TPU > 1 tokens (the layout p.off_*).  A unit is
+// TPU tokens (t0, t0 + 1, ...) and heads
+// [h0, h0 + n) of each; lane 0 fills the ring, and all lanes prefetch the
+// (position, slot) of the tokens of this CTA's next 32 / TPU units (lane L:
+// token L % TPU of the (L / TPU)-th unit on).  The position-independent copies
+// (query rows, key rows, weights) go out before the positions are known.
+static __device__ void producer_multi(const Params& p, unsigned char* ring, uint32_t full0, uint32_t empty0,
+                         volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  const int ub_mask = (32 >> p.tpu_shift) - 1;  // units per prefetch batch, less one
+  long long my_pos = 0, my_slot = 0;
+  // (token unit, chunk) of unit u, advanced incrementally as u steps by gridDim.x
+  const int dt = static_cast<int>(gridDim.x) / p.NC;
+  const int dc = static_cast<int>(gridDim.x) - dt * p.NC;
+  int t = static_cast<int>(blockIdx.x) / p.NC;
+  int c = static_cast<int>(blockIdx.x) - t * p.NC;
+  int i = 0;
+  for (long long u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+    if (i > 0) {
+      t += dt;
+      c += dc;
+      if (c >= p.NC) c -= p.NC, ++t;
+    }
+    const int j = i & ub_mask;
+    if (j == 0) {
+      const long long uu = u + static_cast<long long>(lane >> p.tpu_shift) * gridDim.x;
+      my_pos = 0;
+      my_slot = 0;
+      if (uu < p.units) {
+        const long long tu = uu / p.NC;
+        const long long tt = (tu << p.tpu_shift) + (lane & (p.TPU - 1));
+        if (tt < p.T) {
+          my_pos = __ldg(p.pos + tt);
+          if (uu - tu * p.NC == 0) my_slot = __ldg(p.loc + tt);
+        }
+      }
+    }
+    const long long t0 = static_cast<long long>(t) << p.tpu_shift;
+    const int nt = static_cast<int>(min(static_cast<long long>(p.TPU), p.T - t0));
+    int stop = 0;
+    const int s = i % kStages;
+    const uint32_t full = full0 + 8 * s;
+    unsigned char* st = ring + static_cast<size_t>(s) * p.stage_bytes;
+    const uint32_t sts = smem_u32(st);
+    // test hook: CTA 0 never fills its first stage (see DSA_FLAG_TEST_WITHHOLD_UNIT)
+    const bool withhold = p.test_withhold && blockIdx.x == 0 && i == 0;
+    if (lane == 0) {
+      const uint32_t ph = (i / kStages) & 1;
+      if (i >= kStages && !mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag)) {
+        stop = 1;
+      } else if (!withhold) {
+        const int h0 = c * p.HC;
+        const int n = min(p.HC, p.H - h0);
+        const uint32_t early = static_cast<uint32_t>(nt) *
+                               (static_cast<uint32_t>(n) * 256u + (c == 0 ? 256u : 0u) +
+                                (p.w_bulk ? 2u * n : 0u));
+        if (early) mbar_expect_tx(full, early);
+        if (n > 0) {
+          const uint16_t* qsrc = p.q + t0 * p.sq_t + static_cast<long long>(h0) * p.sq_h;
+          if (p.sq_h == kD && (nt == 1 || p.sq_t == static_cast<long long>(n) * kD)) {
+            bulk_g2s(sts + p.off_q, qsrc, static_cast<uint32_t>(nt * n) * 256u, full);
+          } else if (p.sq_h == kD) {
+            for (int k = 0; k < nt; ++k)
+              bulk_g2s(sts + p.off_q + 256 * n * k, qsrc + k * p.sq_t,
+                       static_cast<uint32_t>(n) * 256u, full);
+          } else {
+            for (int k = 0; k < nt; ++k)
+              for (int h = 0; h < n; ++h)
+                bulk_g2s(sts + p.off_q + 256 * (n * k + h), qsrc + k * p.sq_t + h * p.sq_h, 256u,
+                         full);
+          }
+          if (p.w_bulk) {
+            const uint16_t* wsrc = p.w + t0 * p.sw_t + h0;
+            if (nt == 1 || p.sw_t == n)
+              bulk_g2s(sts + p.off_w, wsrc, static_cast<uint32_t>(nt * n) * 2u, full);
+            else
+              for (int k = 0; k < nt; ++k)
+                bulk_g2s(sts + p.off_w + 2 * n * k, wsrc + k * p.sw_t, 2u * n, full);
+          }
+        }
+        if (c == 0) {
+          if (nt == 1 || p.sk_t == kD)
+            bulk_g2s(sts + p.off_k, p.k + t0 * p.sk_t, static_cast<uint32_t>(nt) * 256u, full);
+          else
+            for (int k = 0; k < nt; ++k)
+              bulk_g2s(sts + p.off_k + 256 * k, p.k + (t0 + k) * p.sk_t, 256u, full);
+        }
+      }
+    }
+    stop = __shfl_sync(kFull, stop, 0);
+    if (stop) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        raise_error(p, DSA_DEVERR_TIMEOUT);
+      }
+      break;
+    }
+    long long pos[kTPUMax], slot[kTPUMax];
+#pragma unroll
+    for (int k = 0; k < kTPUMax; ++k) {
+      if (k < p.TPU) {  // uniform across the warp
+        const int src = (j << p.tpu_shift) + k;
+        pos[k] = __shfl_sync(kFull, my_pos, src);
+        slot[k] = __shfl_sync(kFull, my_slot, src);
+      }
+    }
+    if (lane == 0 && !withhold) {
+      if (p.rope_dim)
+        mbar_arrive_expect_tx(full, 2u * p.cs_bytes * nt);
+#pragma unroll
+      for (int k = 0; k < kTPUMax; ++k) {
+        if (k < nt) {
+          const bool pos_ok = pos[k] >= 0 && pos[k] < p.max_pos;
+          const long long row = pos_ok ? pos[k] : 0;
+          StageHeader* hd = reinterpret_cast<StageHeader*>(st) + k;
+          hd->pos = pos[k];
+          hd->slot = slot[k];
+          hd->pos_ok = pos_ok ? 1 : 0;
+          if (p.rope_dim) {
+            bulk_g2s(sts + p.off_cos + p.cs_bytes * k, p.cos_t + row * p.cs_stride, p.cs_bytes, full);
+            bulk_g2s(sts + p.off_sin + p.cs_bytes * k, p.sin_t + row * p.cs_stride, p.cs_bytes, full);
+          }
+        }
+      }
+      if (!p.rope_dim) mbar_arrive(full);
+    }
+    __syncwarp();
+  }
+  // Stay until the copies of the last (up to kStages) units have landed, so
+  // the CTA never exits with a bulk copy still writing its shared memory.
+  if (lane == 0) {
+    volatile int never = 0;
+    for (int d = (i > kStages ? i - kStages : 0); d < i; ++d)
+      mbar_wait(full0 + 8 * (d % kStages), (d / kStages) & 1, &never);
+  }
+}
+
+// Consumer warp for units of one token (the layout kOff*).
 template <bool HAD, int STYLE, int RP>
-__device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t full0,
+__device__ void consumer_single(const Params& p, int cw, unsigned char* ring, uint32_t full0,
                          uint32_t empty0, volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
   const int qtr = lane >> 3;
@@ -676,7 +823,7 @@ __device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t 
       }
       return;
     }
-    const StageHeader* hd = reinterpret_cast<const StageHeader*>(st + kOffHdr);
+    const StageHeader* hd = reinterpret_cast<const StageHeader*>(st);
     const bool pos_ok = hd->pos_ok != 0;
     const int h0 = c * p.HC;
     const int n = min(p.HC, p.H - h0);
@@ -722,7 +869,127 @@ __device__ void consumer(const Params& p, int cw, unsigned char* ring, uint32_t 
   }
 }
 
+// The rotation operands of token k of a stage.
+template <int RP>
+__device__ __forceinline__ void stage_rot(const Params& p, uint32_t sts, int k, int l, Rot<RP>& r) {
+  if constexpr (RP > 0) {
+    load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(sts + p.off_cos + p.cs_bytes * k + 4 * RP * l, r.c);
+    load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(sts + p.off_sin + p.cs_bytes * k + 4 * RP * l, r.s);
+    finish_rot<RP>(r);
+  }
+}
+
 template <bool HAD, int STYLE, int RP>
+__device__ void consumer_multi(const Params& p, int cw, unsigned char* ring, uint32_t full0,
+                         uint32_t empty0, volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  const int qtr = lane >> 3;
+  const int l = lane & 7;
+  const int dt = static_cast<int>(gridDim.x) / p.NC;
+  const int dc = static_cast<int>(gridDim.x) - dt * p.NC;
+  int t = static_cast<int>(blockIdx.x) / p.NC;
+  int c = static_cast<int>(blockIdx.x) - t * p.NC;
+  int i = 0;
+  for (long long u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+    if (i > 0) {
+      t += dt;
+      c += dc;
+      if (c >= p.NC) c -= p.NC, ++t;
+    }
+    const int s = i % kStages;
+    const uint32_t ph = (i / kStages) & 1;
+    unsigned char* st = ring + static_cast<size_t>(s) * p.stage_bytes;
+    const uint32_t sts = smem_u32(st);
+    const bool ok = mbar_wait(full0 + 8 * s, ph, abort_flag);
+    if (!__all_sync(kFull, ok)) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        raise_error(p, DSA_DEVERR_TIMEOUT);
+      }
+      return;
+    }
+    const StageHeader* hd = reinterpret_cast<const StageHeader*>(st);
+    const long long t0 = static_cast<long long>(t) << p.tpu_shift;
+    const int nt = static_cast<int>(min(static_cast<long long>(p.TPU), p.T - t0));
+    const int h0 = c * p.HC;
+    const int n = min(p.HC, p.H - h0);
+    const int nq = (n + 3) >> 2;  // head quads per token
+
+    // One query head for this quarter-warp: head v of a token whose output
+    // rows start at q_out / w_out, whose query rows start at q_sts in the
+    // stage and whose gate weights start at w_src -- in the stage when they
+    // rode the bulk copy, else in global memory; one generic pointer serves
+    // both.  A quarter-warp past the chunk's last head re-reads it and stores
+    // nothing.
+    auto q_head = [&](int v, uint32_t q_sts, const uint16_t* w_src, uint8_t* q_out, float* w_out,
+                      const Rot<RP>& r, bool pos_ok) {
+      const bool valid = v < n;
+      const int vl = valid ? v : n - 1;
+      float x[16];
+      load_vec<HAD, STYLE, RP, SharedMem>(q_sts + 256 * vl, l, x);
+      const float wv = __uint_as_float(static_cast<uint32_t>(w_src[vl]) << 16);
+      const int e = q_slice<HAD, STYLE, RP>(x, r, q_out + v * kD, l, valid && pos_ok);
+      store_f32_cs(w_out + v, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold),
+                   valid && pos_ok && l == 0);
+    };
+    // token k's bases
+    auto w_base = [&](int k) {
+      return p.w_bulk ? reinterpret_cast<const uint16_t*>(st + p.off_w) + n * k
+                      : p.w + (t0 + k) * p.sw_t + h0;
+    };
+    if (nt == 1) {
+      // one token: its rotation and bases once for the whole unit
+      Rot<RP> r;
+      stage_rot<RP>(p, sts, 0, l, r);
+      const bool pos_ok = hd[0].pos_ok != 0;
+      const long long orow0 = t0 * p.H + h0;
+      uint8_t* const q_out = p.q_out + orow0 * kD;
+      float* const w_out = p.w_out + orow0;
+      const uint16_t* const w_src = w_base(0);
+      const uint32_t q_sts = sts + p.off_q;
+      // query heads: warp cw takes head quads cw, cw + kConsumers, ...
+      for (int qd = cw; qd < nq; qd += kConsumers)
+        q_head(4 * qd + qtr, q_sts, w_src, q_out, w_out, r, pos_ok);
+      // the key rides with chunk 0; the warp that takes it rotates per unit
+      if (c == 0 && cw == i % kConsumers) {
+        float x[16];
+        load_vec<HAD, STYLE, RP, SharedMem>(sts + p.off_k, l, x);
+        k_slice<HAD, STYLE, RP>(p, x, r, l, qtr == 0, pos_ok, hd[0].slot);
+      }
+    } else {
+      // several tokens: warp cw takes token cw % TPU and its head quads
+      // cw / TPU, cw / TPU + 8 / TPU, ...; the token's rotation and bases once
+      const int k = cw & (p.TPU - 1);
+      if (k < nt) {
+        Rot<RP> r;
+        stage_rot<RP>(p, sts, k, l, r);
+        const bool pos_ok = hd[k].pos_ok != 0;
+        const long long orow0 = (t0 + k) * p.H + h0;
+        uint8_t* const q_out = p.q_out + orow0 * kD;
+        float* const w_out = p.w_out + orow0;
+        const uint16_t* const w_src = w_base(k);
+        const uint32_t q_sts = sts + p.off_q + 256 * n * k;
+        for (int qd = cw >> p.tpu_shift; qd < nq; qd += kConsumers >> p.tpu_shift)
+          q_head(4 * qd + qtr, q_sts, w_src, q_out, w_out, r, pos_ok);
+      }
+      // the unit's keys (chunk 0 only): quarter-warp k of one warp takes key k
+      if (c == 0 && cw == i % kConsumers) {
+        const int k = min(qtr, nt - 1);
+        Rot<RP> r;
+        stage_rot<RP>(p, sts, k, l, r);
+        float x[16];
+        load_vec<HAD, STYLE, RP, SharedMem>(sts + p.off_k + 256 * k, l, x);
+        k_slice<HAD, STYLE, RP>(p, x, r, l, qtr < nt, hd[k].pos_ok != 0, hd[k].slot);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+  }
+}
+
+// MULTI: units of several tokens (Params::TPU > 1), else of one token; the
+// two are separate kernels so each gets its own register allocation.
+template <bool HAD, int STYLE, int RP, bool MULTI>
 __global__ void __launch_bounds__(kPipeThreads, HAD ? kPipeCtasHad : kPipeCtas)
     dsa_pipeline_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -744,19 +1011,28 @@ __global__ void __launch_bounds__(kPipeThreads, HAD ? kPipeCtasHad : kPipeCtas)
   grid_dependency_wait();
   grid_launch_dependents();
 
+  // one-token units keep their own lean loops (fixed layout, no token
+  // bookkeeping); units of several tokens take the general ones
   const int warp = threadIdx.x >> 5;
-  if (warp == 0)
-    producer(p, ring, full0, empty0, abort_flag);
-  else
-    consumer<HAD, STYLE, RP>(p, warp - 1, ring, full0, empty0, abort_flag);
+  if constexpr (!MULTI) {
+    if (warp == 0)
+      producer_single(p, ring, full0, empty0, abort_flag);
+    else
+      consumer_single<HAD, STYLE, RP>(p, warp - 1, ring, full0, empty0, abort_flag);
+  } else {
+    if (warp == 0)
+      producer_multi(p, ring, full0, empty0, abort_flag);
+    else
+      consumer_multi<HAD, STYLE, RP>(p, warp - 1, ring, full0, empty0, abort_flag);
+  }
 }
 
 // ---------------------------------------------------------------- kernel tables
 
 using KernelFn = void (*)(Params);
 
-template <bool HAD, int STYLE, int RP>
-constexpr KernelFn pipeline_fn() { return dsa_pipeline_kernel<HAD, STYLE, RP>; }
+template <bool HAD, int STYLE, int RP, bool MULTI = false>
+constexpr KernelFn pipeline_fn() { return dsa_pipeline_kernel<HAD, STYLE, RP, MULTI>; }
 template <bool HAD, int STYLE, int RP>
 constexpr KernelFn direct_fn() { return dsa_direct_kernel<HAD, STYLE, RP>; }
 template <bool HAD, int STYLE, int RP>
@@ -765,6 +1041,7 @@ constexpr KernelFn kstream_fn() { return dsa_kstream_kernel<HAD, STYLE, RP>; }
 // The Hadamard variant's kernels, [rope_style][rope_dim / 16 -> 0, 1, 2, 4, 8];
 // instantiated in their own translation unit.
 extern const KernelFn kPipelineHad[2][5];
+extern const KernelFn kPipelineMultiHad[2][5];
 extern const KernelFn kDirectHad[2][5];
 extern const KernelFn kStreamHad[2][5];
 

@@ -186,3 +186,9 @@ def test_pdl_graph_of_layers_matches_eager(pdl):
         assert np.array_equal(qo.view(torch.uint8).cpu().numpy(), e["q_fp8"])
         assert np.array_equal(wo.cpu().numpy(), e["weights"])
         assert np.array_equal(c.cpu().numpy(), e["cache"])
+
+
+@pytest.mark.parametrize("T,H", [(4001, 16), (3901, 24)])
+def test_multi_token_units(T, H):
+    """The Hadamard variant on units of several tokens (pipeline kernel)."""
+    _check(synth.make_decode(seed=T + H + 7, T=T, H=H, style=(T + H) % 2))

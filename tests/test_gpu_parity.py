@@ -362,6 +362,40 @@ def test_padded_strides_on_both_kernels(kernel):
     assert_parity(inp, ref, run_oracle_qk(inp))
 
 
+@pytest.mark.parametrize("H", [32, 16])
+def test_prefill_full_size_few_heads(H):
+    """Prefill (T = 8192) with 32 and 16 heads: the pipeline kernel packs
+    64 / H tokens into a unit (one bulk copy of their query rows)."""
+    _check(synth.make_prefill(seed=3 + H, H=H))
+
+
+@pytest.mark.parametrize("T,H", [(4001, 13), (3901, 24), (4099, 20), (3699, 8)])
+def test_multi_token_units_ragged(T, H):
+    """Units of several tokens with a ragged last unit, head counts that are
+    not a multiple of 4 or 8 (gate weights from global memory), both
+    pairings."""
+    _check(synth.make_decode(seed=T + H, T=T, H=H, style=(T + H) % 2))
+
+
+@pytest.mark.parametrize("pad_t,pad_h", [(3, 0), (0, 8)])
+def test_multi_token_units_padded_strides(pad_t, pad_h):
+    """Units of several tokens whose query rows are not one contiguous block:
+    a padded token stride (one bulk copy per token) and a padded head stride
+    (one per row); the same bytes as contiguous inputs."""
+    T, H = 3700, 16
+    inp = synth.make_decode(seed=140 + pad_t, T=T, H=H, style=synth.NEOX)
+    d = to_device(inp)
+    ref = run_qk(inp, d, kernel="pipeline")
+    qpad = torch.zeros((T, H + pad_t, 128 + pad_h), dtype=torch.bfloat16, device="cuda")
+    qpad[:, :H, :128] = d["q"]
+    dp_ = dict(d)
+    dp_["q"] = qpad[:, :H, :128]
+    got = run_qk(inp, dp_, kernel="pipeline")
+    for key in ("q_fp8", "weights", "cache"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert_parity(inp, ref, run_oracle_qk(inp))
+
+
 @pytest.mark.parametrize("T,H", [(3, 1000), (2, 4096)])
 def test_many_heads(T, H):
     """Many head chunks per token (the pipeline kernel splits H into chunks
