@@ -142,6 +142,13 @@ void choose_units(Params& p, int sms, bool w_rows_aligned) {
     }
   }
   p.tpu_shift = p.TPU == 4 ? 2 : p.TPU == 2 ? 1 : 0;
+  // fused k|w rows (w = k + 128 elements, one stride, rows of at most 512 B):
+  // one copy per unit brings keys and weights
+  const long long kw_row_b = 2 * p.sk_t;
+  p.kw_fused = (p.TPU > 1 && p.w == p.k + kD && p.sw_t == p.sk_t && kw_row_b % 16 == 0 &&
+                kw_row_b <= 512 && p.H % 8 == 0 && w_rows_aligned) ? 1 : 0;
+  p.kw_row_b = p.kw_fused ? static_cast<int>(kw_row_b) : 256;
+  p.cs_contig = (p.cs_stride == p.rope_dim / 2) ? 1 : 0;
   p.units = (static_cast<long long>(p.T) + p.TPU - 1) / p.TPU * p.NC;
   p.w_bulk = (w_rows_aligned && p.H % 8 == 0 && p.HC % 8 == 0) ? 1 : 0;
   // stage layout: headers (32 B a token), key rows, cos rows, sin rows,
@@ -155,7 +162,7 @@ void choose_units(Params& p, int sms, bool w_rows_aligned) {
     p.off_q = kOffQ;
   } else {
     p.off_k = 32 * p.TPU;
-    p.off_cos = p.off_k + 256 * p.TPU;
+    p.off_cos = p.off_k + p.kw_row_b * p.TPU;
     p.off_sin = p.off_cos + p.cs_bytes * p.TPU;
     p.off_w = p.off_sin + p.cs_bytes * p.TPU;
     p.off_q = (p.off_w + 2 * p.HC * p.TPU + 127) / 128 * 128;

@@ -87,6 +87,12 @@ struct Params {
   // stage layout (byte offsets): per-token headers at 0, then key rows,
   // cos rows, sin rows, gate weights, query rows
   int off_k, off_cos, off_sin, off_w, off_q;
+  // multi-token units: k and w are the fused k|w projection (w = k + 128,
+  // one row stride), so one copy brings a unit's key rows with their
+  // weights; kw_row_b is the rows' stride in the stage (256 when not fused)
+  int kw_fused;
+  int kw_row_b;
+  int cs_contig;  // cos/sin rows are packed (cs_stride == rope_dim / 2)
   // direct kernel
   int NQ;            // quads of heads per token
   long long q_warps;  // warps doing q quads
@@ -549,9 +555,10 @@ constexpr int kOffCos = 320;   // cos row, rope_dim/2 floats (<= 256 B)
 constexpr int kOffSin = 576;   // sin row
 constexpr int kOffW = 832;     // gate weights of the chunk, HC bf16 (<= 128 B)
 constexpr int kOffQ = 1024;    // HC query rows of 256 B
-// the largest stage: headers, key rows, cos and sin rows (<= 256 B each) and
+// the largest stage: headers, key rows (<= 512 B each with fused weights),
+// cos and sin rows (<= 256 B each) and
 // weights of kTPUMax tokens, then query rows of at most kHCMax heads in all
-constexpr int kMaxStageBytes = 32 * kTPUMax + 256 * kTPUMax + 2 * 256 * kTPUMax + 128 + 256 * kHCMax;
+constexpr int kMaxStageBytes = 32 * kTPUMax + 512 * kTPUMax + 2 * 256 * kTPUMax + 128 + 256 * kHCMax;
 
 // Per-token header of a stage.
 struct StageHeader {
@@ -709,9 +716,10 @@ static __device__ void producer_multi(const Params& p, unsigned char* ring, uint
       } else if (!withhold) {
         const int h0 = c * p.HC;
         const int n = min(p.HC, p.H - h0);
-        const uint32_t early = static_cast<uint32_t>(nt) *
-                               (static_cast<uint32_t>(n) * 256u + (c == 0 ? 256u : 0u) +
-                                (p.w_bulk ? 2u * n : 0u));
+        // query rows; key rows (with their weights when fused); weights
+        const uint32_t kw_bytes = p.kw_fused ? static_cast<uint32_t>((nt - 1) * p.kw_row_b + 256 + 2 * n)
+                                             : 256u * nt + (p.w_bulk ? 2u * n * nt : 0u);
+        const uint32_t early = static_cast<uint32_t>(nt * n) * 256u + (c == 0 ? kw_bytes : 0u);
         if (early) mbar_expect_tx(full, early);
         if (n > 0) {
           const uint16_t* qsrc = p.q + t0 * p.sq_t + static_cast<long long>(h0) * p.sq_h;
@@ -727,7 +735,7 @@ static __device__ void producer_multi(const Params& p, unsigned char* ring, uint
                 bulk_g2s(sts + p.off_q + 256 * (n * k + h), qsrc + k * p.sq_t + h * p.sq_h, 256u,
                          full);
           }
-          if (p.w_bulk) {
+          if (p.w_bulk && !p.kw_fused) {
             const uint16_t* wsrc = p.w + t0 * p.sw_t + h0;
             if (nt == 1 || p.sw_t == n)
               bulk_g2s(sts + p.off_w, wsrc, static_cast<uint32_t>(nt * n) * 2u, full);
@@ -737,7 +745,9 @@ static __device__ void producer_multi(const Params& p, unsigned char* ring, uint
           }
         }
         if (c == 0) {
-          if (nt == 1 || p.sk_t == kD)
+          if (p.kw_fused)  // rows t0.. of the k|w buffer: keys, weights and what lies between
+            bulk_g2s(sts + p.off_k, p.k + t0 * p.sk_t, kw_bytes, full);
+          else if (nt == 1 || p.sk_t == kD)
             bulk_g2s(sts + p.off_k, p.k + t0 * p.sk_t, static_cast<uint32_t>(nt) * 256u, full);
           else
             for (int k = 0; k < nt; ++k)
@@ -765,22 +775,38 @@ static __device__ void producer_multi(const Params& p, unsigned char* ring, uint
     if (lane == 0 && !withhold) {
       if (p.rope_dim)
         mbar_arrive_expect_tx(full, 2u * p.cs_bytes * nt);
+      // consecutive in-range positions over packed rows: one copy each of
+      // the unit's cos rows and sin rows (prefill), else one per token
+      bool consec = p.cs_contig != 0;
 #pragma unroll
       for (int k = 0; k < kTPUMax; ++k) {
         if (k < nt) {
           const bool pos_ok = pos[k] >= 0 && pos[k] < p.max_pos;
-          const long long row = pos_ok ? pos[k] : 0;
+          consec = consec && pos_ok && pos[k] == pos[0] + k;
           StageHeader* hd = reinterpret_cast<StageHeader*>(st) + k;
           hd->pos = pos[k];
           hd->slot = slot[k];
           hd->pos_ok = pos_ok ? 1 : 0;
-          if (p.rope_dim) {
-            bulk_g2s(sts + p.off_cos + p.cs_bytes * k, p.cos_t + row * p.cs_stride, p.cs_bytes, full);
-            bulk_g2s(sts + p.off_sin + p.cs_bytes * k, p.sin_t + row * p.cs_stride, p.cs_bytes, full);
-          }
         }
       }
-      if (!p.rope_dim) mbar_arrive(full);
+      if (p.rope_dim) {
+        if (consec) {
+          const uint32_t bytes = static_cast<uint32_t>(p.cs_bytes * nt);
+          bulk_g2s(sts + p.off_cos, p.cos_t + pos[0] * p.cs_stride, bytes, full);
+          bulk_g2s(sts + p.off_sin, p.sin_t + pos[0] * p.cs_stride, bytes, full);
+        } else {
+#pragma unroll
+          for (int k = 0; k < kTPUMax; ++k) {
+            if (k < nt) {
+              const long long row = (pos[k] >= 0 && pos[k] < p.max_pos) ? pos[k] : 0;
+              bulk_g2s(sts + p.off_cos + p.cs_bytes * k, p.cos_t + row * p.cs_stride, p.cs_bytes, full);
+              bulk_g2s(sts + p.off_sin + p.cs_bytes * k, p.sin_t + row * p.cs_stride, p.cs_bytes, full);
+            }
+          }
+        }
+      } else {
+        mbar_arrive(full);
+      }
     }
     __syncwarp();
   }
@@ -932,10 +958,12 @@ __device__ void consumer_multi(const Params& p, int cw, unsigned char* ring, uin
       store_f32_cs(w_out + v, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold),
                    valid && pos_ok && l == 0);
     };
-    // token k's bases
+    // token k's weights: beside its key row (fused k|w), in the weights
+    // region, or in global memory
     auto w_base = [&](int k) {
-      return p.w_bulk ? reinterpret_cast<const uint16_t*>(st + p.off_w) + n * k
-                      : p.w + (t0 + k) * p.sw_t + h0;
+      return p.kw_fused ? reinterpret_cast<const uint16_t*>(st + p.off_k + p.kw_row_b * k + 2 * kD)
+             : p.w_bulk ? reinterpret_cast<const uint16_t*>(st + p.off_w) + n * k
+                        : p.w + (t0 + k) * p.sw_t + h0;
     };
     if (nt == 1) {
       // one token: its rotation and bases once for the whole unit
@@ -978,7 +1006,7 @@ __device__ void consumer_multi(const Params& p, int cw, unsigned char* ring, uin
         Rot<RP> r;
         stage_rot<RP>(p, sts, k, l, r);
         float x[16];
-        load_vec<HAD, STYLE, RP, SharedMem>(sts + p.off_k + 256 * k, l, x);
+        load_vec<HAD, STYLE, RP, SharedMem>(sts + p.off_k + p.kw_row_b * k, l, x);
         k_slice<HAD, STYLE, RP>(p, x, r, l, qtr < nt, hd[k].pos_ok != 0, hd[k].slot);
       }
     }
