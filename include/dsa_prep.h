@@ -297,9 +297,10 @@ dsa_status dsa_indexer_qk_prepare_store_unfused_noalloc(
  *   q_fp8          e4m3 [T, H, 128] contiguous, 16-byte aligned.
  *   weights        fp32 [T, H] contiguous.
  *   index_k_cache  page-blocked layout, page_size == 64, 16-byte aligned.
- *   block_table    int32 [T, >= ceil(min(context_lens[t], max_context) / 64)],
- *                  row stride bt_stride: the physical page of each 64-key
- *                  block.
+ *   block_table    int32 [T, bt_stride], bt_stride >= ceil(max_context / 64)
+ *                  (else DSA_ERR_SHAPE): the physical page of each 64-key
+ *                  block.  A row's entries past its token's context are read
+ *                  and ignored, so they may hold anything.
  *   context_lens   int32 [T], keys of token t; only the first max_context
  *                  of them have a column (a longer context is clamped).
  *   logits         fp32 [T, logits_stride >= max_context].
@@ -307,7 +308,8 @@ dsa_status dsa_indexer_qk_prepare_store_unfused_noalloc(
  *   with it, DSA_FLAG_PDL_EARLY_INDEX.
  * Runs on the tensor cores (tcgen05, fp32 accumulation in TMEM); the first
  * call on a device raises its shared-memory limit there.  A block-table entry
- * outside [0, num_pages) sets DSA_DEVERR_SLOT (its keys then read page 0).
+ * (within the context) outside [0, num_pages) sets DSA_DEVERR_SLOT, and its
+ * keys' logits are NaN.
  */
 dsa_status dsa_indexer_mqa_logits(
     const void* q_fp8, const float* weights,

@@ -57,6 +57,7 @@ struct LParams {
   int tiles_max;  // ceil(max_context / 128)
   int T;
   int early_index;  // read context_lens / block_table before the PDL wait
+                    // (also every launch without PDL: nothing runs before it)
   int* err;
 };
 
@@ -226,14 +227,17 @@ __global__ void __launch_bounds__(kLThreads, 1)
   int cur[2 * kBatch];
   int len = 0;
   if (p.early_index) {
-    // DSA_FLAG_PDL_EARLY_INDEX: the context length and the block table are
-    // not written by the previous kernel.  The producer also starts its first
-    // pages on their way into L2 (a hint, coherent with any write the
-    // previous kernel makes to them) while that kernel finishes.
+    // DSA_FLAG_PDL_EARLY_INDEX (or no PDL): the context length and the block
+    // table are not written by the previous kernel.  The first batch of the
+    // table is read without waiting for the length (bounded by max_context,
+    // which the table covers), and the producer starts its first pages on
+    // their way into L2 (a hint, coherent with any write the previous kernel
+    // makes to them) while that kernel finishes.
+    if (warp == 0 && lane == 0)
+      load_batch(static_cast<int>(blockIdx.x), p.tiles_max, p.max_context, cur);
     len = context_of(t);
     if (warp == 0 && lane == 0) {
       const int nt = tiles_of(len);
-      load_batch(static_cast<int>(blockIdx.x), nt, len, cur);
 #pragma unroll
       for (int k = 0; k < kKStages; ++k) {
         const int i = static_cast<int>(blockIdx.x) + k * step;
@@ -280,20 +284,33 @@ __global__ void __launch_bounds__(kLThreads, 1)
             break;
           }
           const bool has1 = (2 * i + 1) * kPageKeys < len;
-          mbar_arrive_expect_tx(full(s), (has1 ? 2 : 1) * (kPageBytes + kPageKeys * 4));
           const uint32_t dst = sbase + L::kOffK + s * kTileBytes;
           const uint32_t sdst = sbase + L::kOffS + s * kTileKeys * 4;
-          auto load_page = [&](int h, long long pg) {
-            if (pg < 0 || pg >= p.num_pages) {
-              if (p.err) atomicOr(p.err, DSA_DEVERR_SLOT);
-              pg = 0;
-            }
-            tma_load_3d(dst + h * kPageBytes, &tk, 0, 0, static_cast<int>(pg), full(s));
-            bulk_g2s(sdst + h * kPageKeys * 4, p.cache + pg * kPageStride + kPageBytes,
-                     kPageKeys * 4, full(s));
+          // A page outside [0, num_pages) sets the error bit; its keys' logits
+          // are NaN, as the oracle defines them: the MMA still takes page 0's
+          // codes, but the stage gets NaN scales, stored before the arrival
+          // below publishes them, instead of a copy.
+          const long long pg0 = cur[2 * k], pg1 = cur[2 * k + 1];
+          const bool bad0 = pg0 < 0 || pg0 >= p.num_pages;
+          const bool bad1 = has1 && (pg1 < 0 || pg1 >= p.num_pages);
+          if (bad0 || bad1) {
+            if (p.err) atomicOr(p.err, DSA_DEVERR_SLOT);
+            for (int h = 0; h < 2; ++h)
+              if (h == 0 ? bad0 : bad1)
+                for (int q = 0; q < kPageKeys; q += 4)
+                  asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
+                               ::"r"(sdst + 4 * (h * kPageKeys + q)), "r"(0x7fc00000) : "memory");
+          }
+          const int scales = (bad0 ? 0 : 1) + (has1 && !bad1 ? 1 : 0);
+          mbar_arrive_expect_tx(full(s), (has1 ? 2 : 1) * kPageBytes + scales * kPageKeys * 4);
+          auto load_page = [&](int h, long long pg, bool bad) {
+            tma_load_3d(dst + h * kPageBytes, &tk, 0, 0, bad ? 0 : static_cast<int>(pg), full(s));
+            if (!bad)
+              bulk_g2s(sdst + h * kPageKeys * 4, p.cache + pg * kPageStride + kPageBytes,
+                       kPageKeys * 4, full(s));
           };
-          load_page(0, cur[2 * k]);
-          if (has1) load_page(1, cur[2 * k + 1]);
+          load_page(0, pg0, bad0);
+          if (has1) load_page(1, pg1, bad1);
           ++m;
         }
 #pragma unroll
@@ -535,6 +552,10 @@ dsa_status dsa_indexer_mqa_logits(const void* q_fp8, const float* weights,
   if (num_pages > 0x7fffffffLL || static_cast<long long>(T) * H > 0x7fffffffLL)
     return DSA_ERR_SHAPE;
   if (logits_stride < max_context) return DSA_ERR_SHAPE;
+  // every row of the table covers max_context keys (the kernel may read a
+  // row's first blocks before it knows the token's context length)
+  if (bt_stride < (static_cast<long long>(max_context) + kPageKeys - 1) / kPageKeys)
+    return DSA_ERR_SHAPE;
   if (T == 0 || max_context == 0) return DSA_OK;
   if (!q_fp8 || !weights || !index_k_cache || !block_table || !context_lens || !logits)
     return DSA_ERR_NULL;
@@ -588,7 +609,9 @@ dsa_status dsa_indexer_mqa_logits(const void* q_fp8, const float* weights,
   p.max_context = max_context;
   p.tiles_max = (max_context + kTileKeys - 1) / kTileKeys;
   p.T = T;
-  p.early_index = (flags & DSA_FLAG_PDL_EARLY_INDEX) ? 1 : 0;
+  // A launch without PDL starts once the previous kernel has finished, so
+  // it may read the lengths and the table at once, as the early mode does.
+  p.early_index = ((flags & DSA_FLAG_PDL_EARLY_INDEX) || !(flags & DSA_FLAG_PDL)) ? 1 : 0;
   p.err = err_flags;
   // split each token's tiles over as many CTAs as fit on the GPU at once
   // (all resident: no second wave), at least one per token

@@ -146,6 +146,7 @@ def _lg(lib, **over):
     (dict(flags=64), 4),  # DSA_FLAG_PDL_EARLY_INDEX needs DSA_FLAG_PDL
     (dict(q=None), 1), (dict(lens=None), 1), (dict(q=A + 8), 2), (dict(cache=A + 4), 2),
     (dict(w=A + 2), 2),
+    (dict(bts=1), 3), (dict(maxc=257, outs=300, bts=4), 3),  # rows must cover max_context
 ])
 def test_logits_validation(lib, over, status):
     assert _lg(lib, **over) == status
