@@ -41,6 +41,9 @@
  *   - Pointers are DEVICE pointers owned by the caller; the library allocates
  *     nothing, keeps no state between calls and caches no pointer or table
  *     contents (a replaced cos/sin cache is read afresh on the next call).
+ *   - A call acts on the current CUDA device: the stream and every pointer
+ *     must belong to it (the SM count and kernel attributes are that
+ *     device's).
  *   - Strides are in elements.  The innermost dimension of q, k and w is
  *     contiguous.
  *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
@@ -102,10 +105,12 @@ typedef enum { DSA_ROPE_NEOX = 0, DSA_ROPE_GPTJ = 1 } dsa_rope_style;
                            waits for that kernel's memory before reading
                            anything */
 /* Kernel choice.  By default calls with T * H <= 16384 query vectors take the
- * direct kernel (loads straight to registers: least latency, for decode) and
- * larger ones the pipeline kernel (bulk copies through a shared-memory ring:
- * most bandwidth, for prefill); the k-only call always takes the direct
- * kernel.  These flags force one; both give the same bytes.  Setting both is
+ * direct kernel (every input in flight at once: least latency, for decode)
+ * and larger ones the pipeline kernel (bulk copies through a shared-memory
+ * ring: most bandwidth, for prefill).  k-only calls take the direct kernel up
+ * to 8192 keys and the k-stream kernel (persistent warps over key ranges,
+ * cp.async rings) above; for them DSA_FLAG_PIPELINE selects the k-stream
+ * kernel.  These flags force one; all give the same bytes.  Setting both is
  * an error. */
 #define DSA_FLAG_PIPELINE 2u
 #define DSA_FLAG_DIRECT 4u
@@ -260,7 +265,9 @@ dsa_status dsa_indexer_qk_prepare_store_unfused(
  * The caller still passes all inputs and outputs; the call allocates nothing
  * (no cudaMalloc or cudaFree).  The first call on each device looks the
  * buffer's device address up once, with that device current -- make that
- * first call outside any stream capture.
+ * first call outside any stream capture.  The address is kept for the life
+ * of the process: after a cudaDeviceReset of a device this entry point has
+ * run on, the kept address is stale, so do not call it on that device again.
  *
  * All calls on a device share the one buffer: two calls that may run on the
  * GPU at the same time (different streams without ordering between them)

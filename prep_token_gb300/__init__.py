@@ -15,6 +15,7 @@ fold, and the paged index-K cache write.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -178,6 +179,15 @@ def _err_ptr(err_flags, device):
     return err_flags.data_ptr()
 
 
+def _on(device):
+    """The tensors' device made current for a library call (the C side takes
+    the SM count, kernel attributes and scratch address from the current
+    device); a no-op when it already is."""
+    if device.index is None or torch.cuda.current_device() == device.index:
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
 def _stream(stream, device=None) -> int:
     if stream is None:
         return torch.cuda.current_stream(device).cuda_stream
@@ -278,9 +288,10 @@ def dsa_indexer_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, s
                                 ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
                                 page_size, rope_dim, rope_style, q_fp8_out, weights_out,
                                 num_tokens, max_position)
-    st = library().dsa_indexer_qk_prepare_store(
-        *args, _flags(pdl, kernel) | _layout(cache_layout) | (FLAG_HADAMARD if hadamard else 0),
-        _err_ptr(err_flags, q.device), _stream(stream, q.device))
+    with _on(q.device):
+        st = library().dsa_indexer_qk_prepare_store(
+            *args, _flags(pdl, kernel) | _layout(cache_layout) | (FLAG_HADAMARD if hadamard else 0),
+            _err_ptr(err_flags, q.device), _stream(stream, q.device))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store")
     return outs
@@ -313,9 +324,10 @@ def dsa_indexer_qk_prepare_store_unfused(q, k, w, positions, out_cache_loc, cos_
             or not workspace.is_contiguous():
         raise ValueError(f"workspace must be a contiguous tensor on {q.device}")
     nbytes = workspace.numel() * workspace.element_size()
-    st = library().dsa_indexer_qk_prepare_store_unfused(
-        *args, (FLAG_PDL if pdl else 0) | _layout(cache_layout), _ptr(workspace), nbytes,
-        _err_ptr(err_flags, q.device), _stream(stream, q.device))
+    with _on(q.device):
+        st = library().dsa_indexer_qk_prepare_store_unfused(
+            *args, (FLAG_PDL if pdl else 0) | _layout(cache_layout), _ptr(workspace), nbytes,
+            _err_ptr(err_flags, q.device), _stream(stream, q.device))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store_unfused")
     return outs
@@ -341,9 +353,10 @@ def dsa_indexer_qk_prepare_store_unfused_noalloc(q, k, w, positions, out_cache_l
                                 ln_gamma, ln_beta, ln_eps, softmax_scale, index_k_cache,
                                 page_size, rope_dim, rope_style, q_fp8_out, weights_out,
                                 num_tokens, max_position)
-    st = library().dsa_indexer_qk_prepare_store_unfused_noalloc(
-        *args, (FLAG_PDL if pdl else 0) | _layout(cache_layout), _err_ptr(err_flags, q.device),
-        _stream(stream, q.device))
+    with _on(q.device):
+        st = library().dsa_indexer_qk_prepare_store_unfused_noalloc(
+            *args, (FLAG_PDL if pdl else 0) | _layout(cache_layout), _err_ptr(err_flags, q.device),
+            _stream(stream, q.device))
     if st != 0:
         raise DsaError(st, "dsa_indexer_qk_prepare_store_unfused_noalloc")
     return outs
@@ -377,9 +390,10 @@ def dsa_indexer_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cach
     ``hadamard=True`` rotates k by H_128 / sqrt(128) after RoPE."""
     args = _k_args(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta, ln_eps,
                    index_k_cache, page_size, rope_dim, rope_style, num_tokens, max_position)
-    st = library().dsa_indexer_k_prepare_store(
-        *args, _flags(pdl, kernel) | _layout(cache_layout) | (FLAG_HADAMARD if hadamard else 0),
-        _err_ptr(err_flags, k.device), _stream(stream, k.device))
+    with _on(k.device):
+        st = library().dsa_indexer_k_prepare_store(
+            *args, _flags(pdl, kernel) | _layout(cache_layout) | (FLAG_HADAMARD if hadamard else 0),
+            _err_ptr(err_flags, k.device), _stream(stream, k.device))
     if st != 0:
         raise DsaError(st, "dsa_indexer_k_prepare_store")
 
@@ -395,15 +409,17 @@ class PreparedCall:
     preparation, and the call raises DsaError on a non-zero status.  Calling
     it returns the outputs it writes (for the fused call: q_fp8, weights)."""
 
-    def __init__(self, fn, name, args, outs=None, keep=()):
+    def __init__(self, fn, name, args, device, outs=None, keep=()):
         self._fn = fn
         self._name = name
+        self._device = device
         self._args = tuple(t(a) if a is not None else None for t, a in zip(fn.argtypes, args))
         self._outs = outs
         self._keep = keep  # tensors whose pointers the arguments hold
 
     def __call__(self):
-        st = self._fn(*self._args)
+        with _on(self._device):
+            st = self._fn(*self._args)
         if st != 0:
             raise DsaError(st, self._name)
         return self._outs
@@ -425,7 +441,7 @@ def prepare_qk_prepare_store(q, k, w, positions, out_cache_loc, cos_cache, sin_c
             _err_ptr(err_flags, q.device), _stream(stream, q.device))
     keep = (q, k, w, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta,
             index_k_cache, err_flags) + tuple(outs)
-    return PreparedCall(fn, "dsa_indexer_qk_prepare_store", full, outs, keep)
+    return PreparedCall(fn, "dsa_indexer_qk_prepare_store", full, q.device, outs, keep)
 
 
 def prepare_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta,
@@ -440,7 +456,7 @@ def prepare_k_prepare_store(k, positions, out_cache_loc, cos_cache, sin_cache, l
             _err_ptr(err_flags, k.device), _stream(stream, k.device))
     keep = (k, positions, out_cache_loc, cos_cache, sin_cache, ln_gamma, ln_beta, index_k_cache,
             err_flags)
-    return PreparedCall(fn, "dsa_indexer_k_prepare_store", full, None, keep)
+    return PreparedCall(fn, "dsa_indexer_k_prepare_store", full, k.device, None, keep)
 
 
 def dsa_indexer_mqa_logits(q_fp8, weights, index_k_cache, page_size, block_table, context_lens,
@@ -482,12 +498,13 @@ def dsa_indexer_mqa_logits(q_fp8, weights, index_k_cache, page_size, block_table
     _need(logits, "logits", torch.float32, 2, dev)
     if logits.shape[0] < T:
         raise ValueError(f"logits has fewer than {T} rows")
-    st = library().dsa_indexer_mqa_logits(
-        _ptr(q_fp8), _ptr(weights), _ptr(index_k_cache), _num_pages(index_k_cache, page_size),
-        page_size, _ptr(block_table), block_table.stride(0), _ptr(context_lens), _ptr(logits),
-        logits.stride(0), int(max_context), T, H,
-        (FLAG_PDL if pdl else 0) | (FLAG_PDL_EARLY_INDEX if pdl == "early" else 0), _err_ptr(err_flags, q_fp8.device),
-        _stream(stream, q_fp8.device))
+    with _on(q_fp8.device):
+        st = library().dsa_indexer_mqa_logits(
+            _ptr(q_fp8), _ptr(weights), _ptr(index_k_cache), _num_pages(index_k_cache, page_size),
+            page_size, _ptr(block_table), block_table.stride(0), _ptr(context_lens), _ptr(logits),
+            logits.stride(0), int(max_context), T, H,
+            (FLAG_PDL if pdl else 0) | (FLAG_PDL_EARLY_INDEX if pdl == "early" else 0), _err_ptr(err_flags, q_fp8.device),
+            _stream(stream, q_fp8.device))
     if st != 0:
         raise DsaError(st, "dsa_indexer_mqa_logits")
     return logits[:, :max_context]

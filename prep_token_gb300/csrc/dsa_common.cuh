@@ -659,9 +659,22 @@ __device__ __forceinline__ void affine_piece(const float* g_row, const float* b_
   load_f32_global<N, ALIGN>(g_row, g);
   load_f32_global<N, ALIGN>(b_row, b);
 #pragma unroll
-  for (int m = 0; m < M; ++m)
+  for (int m = 0; m < M; ++m) {
+    if (N % 2 == 0 && at % 2 == 0) {  // two elements per packed instruction
+      const float2 r2 = make_float2(rstd[m], rstd[m]);
 #pragma unroll
-    for (int j = 0; j < N; ++j) x[m][at + j] = __fmaf_rn(__fmul_rn(x[m][at + j], rstd[m]), g[j], b[j]);
+      for (int j = 0; j < N; j += 2) {
+        const float2 y = __ffma2_rn(__fmul2_rn(make_float2(x[m][at + j], x[m][at + j + 1]), r2),
+                                    make_float2(g[j], g[j + 1]), make_float2(b[j], b[j + 1]));
+        x[m][at + j] = y.x;
+        x[m][at + j + 1] = y.y;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < N; ++j)
+        x[m][at + j] = __fmaf_rn(__fmul_rn(x[m][at + j], rstd[m]), g[j], b[j]);
+    }
+  }
 }
 
 template <int STYLE, int RP, int M>

@@ -63,3 +63,42 @@ def test_noalloc_rejects_calls_beyond_its_buffer():
         _call(dp.dsa_indexer_qk_prepare_store_unfused_noalloc, inp, d, q_out, w_out, cache)
     assert exc.value.status == 6
     assert torch.all(cache == SENTINEL)
+
+
+def test_noalloc_at_its_exact_limit():
+    """T * (H + 2) * 256 bytes equal to the 32 MiB buffer: accepted, and the
+    same bytes as the workspace entry point."""
+    import prep_token_gb300 as dp
+    inp = synth.make_decode(seed=43, T=2048, H=62, style=synth.NEOX)
+    assert dp.dsa_unfused_workspace_bytes(inp.T, inp.H) == 32 << 20
+    d = to_device(inp)
+    ref = _call(dp.dsa_indexer_qk_prepare_store_unfused, inp, d, *_outputs(inp))
+    got = _call(dp.dsa_indexer_qk_prepare_store_unfused_noalloc, inp, d, *_outputs(inp))
+    for key in ("q_fp8", "weights", "cache"):
+        assert np.array_equal(got[key], ref[key]), key
+
+
+def test_noalloc_two_pdl_calls_in_a_row():
+    """Two calls with programmatic dependent launch back to back on one
+    stream share the buffer in turn (each launch waits for the one before):
+    both give the eager bytes."""
+    import prep_token_gb300 as dp
+    a = synth.make_decode(seed=44, T=64, H=64)
+    b = synth.make_decode(seed=45, T=64, H=64)
+    da, db = to_device(a), to_device(b)
+    ref_a = _call(dp.dsa_indexer_qk_prepare_store_unfused, a, da, *_outputs(a))
+    ref_b = _call(dp.dsa_indexer_qk_prepare_store_unfused, b, db, *_outputs(b))
+    outs_a, outs_b = _outputs(a), _outputs(b)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for inp, d, (q_out, w_out, cache) in ((a, da, outs_a), (b, db, outs_b)):
+            dp.dsa_indexer_qk_prepare_store_unfused_noalloc(
+                d["q"], d["k"], d["w"], d["positions"], d["slots"], d["cos"], d["sin"],
+                d["gamma"], d["beta"], inp.eps, inp.softmax_scale, cache, inp.page_size,
+                inp.rope_dim, inp.style, q_fp8_out=q_out, weights_out=w_out,
+                max_position=inp.max_position, pdl=True, stream=s)
+    s.synchronize()
+    for ref, (q_out, w_out, cache) in ((ref_a, outs_a), (ref_b, outs_b)):
+        assert np.array_equal(q_out.view(torch.uint8).cpu().numpy(), ref["q_fp8"])
+        assert np.array_equal(w_out.cpu().numpy(), ref["weights"])
+        assert np.array_equal(cache.cpu().numpy(), ref["cache"])
