@@ -193,11 +193,14 @@ __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const R
 // and beta read piece by piece from global memory (k_slice<..., false>), each
 // phase run for all N keys before the next so their dependent chains
 // interleave, and each gamma/beta piece loaded once for all N.  Per key the
-// arithmetic is k_slice's, so the bytes written are the same.
+// arithmetic is k_slice's, so the bytes written are the same.  The caller
+// has resolved each key's slot: `code` and `scale` are where its 128 codes
+// and its scale go, `store` whether they are written, and `err` the error
+// bit it raises (0 for none).
 template <bool HAD, int STYLE, int RP, int N>
 __device__ __forceinline__ void k_multi(const Params& p, float (&x)[N][16], const Rot<RP> (&r)[N],
-                                        int l, const bool (&real)[N], const bool (&pos_ok)[N],
-                                        const long long (&slot)[N]) {
+                                        int l, uint8_t* const (&code)[N], float* const (&scale)[N],
+                                        const bool (&store)[N], const int (&err)[N]) {
   float rstd[N];
 #pragma unroll
   for (int n = 0; n < N; ++n) rstd[n] = ln_center(x[n], p.eps);
@@ -221,14 +224,12 @@ __device__ __forceinline__ void k_multi(const Params& p, float (&x)[N][16], cons
   }
 #pragma unroll
   for (int n = 0; n < N; ++n) {
-    const bool slot_ok = slot[n] >= 0 && slot[n] < p.cg.num_slots;
-    if (real[n] && l == 0 && !(pos_ok[n] && slot_ok))
-      raise_error(p, pos_ok[n] ? DSA_DEVERR_SLOT : DSA_DEVERR_POSITION);
-    const bool store = real[n] && pos_ok[n] && slot_ok;
+    if (err[n] && l == 0) raise_error(p, err[n]);
     if constexpr (HAD)
-      store_index_k_h<STYLE, RP>(p.cg, store ? slot[n] : 0, l, wa[n], e[n], store);
+      store_hslice<STYLE, RP, 4>(code[n], l, wa[n], store[n]);
     else
-      store_index_k<STYLE, RP>(p.cg, store ? slot[n] : 0, l, wa[n], wb[n], wp[n], e[n], store);
+      store_slice<STYLE, RP, 4>(code[n], l, wa[n], wb[n], wp[n], store[n]);
+    store_f32(scale[n], pow2f(e[n]), store[n] && l == 0);
   }
 }
 
@@ -366,12 +367,15 @@ __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params
 // Large k-only calls (the decode fast path's key store at prefill size):
 // persistent CTAs whose warps each own a contiguous range of keys, walked in
 // steps of kStreamKeys keys -- kStreamKPQ per quarter-warp, computed together
-// by k_multi.  Each lane holds the position and slot of one key of the warp's
-// current batch of 32 (and prefetches the next batch), so every input of a
-// step -- the key rows and their cos/sin row slices -- is copied by cp.async
-// into a stage of the warp's shared-memory ring kStreamStages - 1 steps ahead
-// of the math.  Per key the arithmetic is that of the other kernels, so every
-// kernel writes the same bytes.
+// by k_multi.  Keys come in batches of 32: when a batch becomes current, lane
+// L resolves key L -- its position and slot, the offset of its cos/sin row,
+// the cache bytes of its codes and its scale, and whether it is in range --
+// into a per-warp table in shared memory (two batches deep), so no lane
+// repeats that scalar work for its key.  Every input of a step -- the key
+// rows and their cos/sin row slices -- is copied by cp.async into a stage of
+// the warp's shared-memory ring kStreamStages - 1 steps ahead of the math.
+// Per key the arithmetic is that of the other kernels, so every kernel
+// writes the same bytes.
 constexpr int kStreamKPQ = 2;                 // keys per quarter-warp per step
 constexpr int kStreamKeys = 4 * kStreamKPQ;   // keys per warp per step
 constexpr int kStreamWarps = 8;
@@ -379,25 +383,39 @@ constexpr int kStreamThreads = 32 * kStreamWarps;
 constexpr int kStreamStages = 2;              // the step computed and the one in flight
 constexpr int kStreamCtas = 2;                // resident CTAs per SM the grid is sized for
 
+// A key resolved for the k-stream kernel (one per lane of a batch).
+struct StreamKey {
+  long long cs_off;     // element offset of its cos/sin row
+  long long code_off;   // cache byte offset of its 128 codes
+  long long scale_off;  // cache byte offset of its scale
+  int store;            // position and slot in range
+  int err;              // the error bit it raises, or 0
+};
+
 // Stage layout (bytes): kStreamKeys key rows ROW bytes apart, then the cos
 // and the sin slices of those keys (32 * RP bytes each: lane l's RP values at
-// 4 * RP * l), then per key its slot and whether its position is in range.
-// Key u of a step sits in quarter-warp u % 4.  ROW = 256 + 64 puts the rows of
-// quarter-warps 0 and 1 (and 2 and 3) in different banks, so an 8-byte slice
-// load of the whole warp takes two shared-memory wavefronts, not four.
+// 4 * RP * l).  Key u of a step sits in quarter-warp u % 4.  ROW = 256 + 64
+// puts the rows of quarter-warps 0 and 1 (and 2 and 3) in different banks, so
+// an 8-byte slice load of the whole warp takes two shared-memory wavefronts,
+// not four.
 template <int RP>
 struct StreamStage {
   static constexpr int ROW = 2 * kD + 64;
   static constexpr int CS = 32 * RP;  // cos (or sin) bytes of one key
   static constexpr int COS = kStreamKeys * ROW;
   static constexpr int SIN = COS + kStreamKeys * CS;
-  static constexpr int IDX = SIN + kStreamKeys * CS;
-  static constexpr int BYTES = IDX + kStreamKeys * 16;
+  static constexpr int BYTES = SIN + kStreamKeys * CS;
 };
 
+// per warp: the ring, then two batches of resolved keys
 template <int RP>
-constexpr int kstream_smem() {
-  return kStreamWarps * kStreamStages * StreamStage<RP>::BYTES;
+__host__ __device__ constexpr int kstream_warp_bytes() {
+  return kStreamStages * StreamStage<RP>::BYTES + 2 * 32 * static_cast<int>(sizeof(StreamKey));
+}
+
+template <int RP>
+__host__ __device__ constexpr int kstream_smem() {
+  return kStreamWarps * kstream_warp_bytes<RP>();
 }
 
 // cp.async of the lane's RP fp32 values (4 * RP bytes, aligned to that or 16).
@@ -434,8 +452,9 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
   const int n = k0 < k1 ? static_cast<int>((k1 - k0 + kStreamKeys - 1) / kStreamKeys) : 0;
   grid_launch_dependents();
   grid_dependency_wait();
-  const uint32_t ring = smem_u32(smem) + wi * kStreamStages * SS::BYTES;
-  unsigned char* ring_p = smem + wi * kStreamStages * SS::BYTES;
+  unsigned char* const wbase = smem + wi * kstream_warp_bytes<RP>();
+  const uint32_t ring = smem_u32(wbase);
+  StreamKey* const keys = reinterpret_cast<StreamKey*>(wbase + kStreamStages * SS::BYTES);
 
   // position and slot of key k0 + 32 b + lane (clamped into the range)
   auto batch = [&](int b, long long& pos, long long& slot) {
@@ -444,17 +463,38 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
     pos = __ldg(p.pos + t);
     slot = __ldg(p.loc + t);
   };
-  long long b_pos = 0, b_slot = 0, nb_pos = 0, nb_slot = 0;
-  if (n > 0) {  // the loads go out now; the first shuffle of b_pos waits for them
-    batch(0, b_pos, b_slot);
+  // Lane L resolves key L of batch b into the table (slot b % 2).
+  auto resolve = [&](int b, long long pos, long long slot) {
+    StreamKey kk;
+    const bool pos_ok = pos >= 0 && pos < p.max_pos;
+    const bool slot_ok = slot >= 0 && slot < p.cg.num_slots;
+    kk.cs_off = (pos_ok ? pos : 0) * p.cs_stride;
+    const long long sl = slot_ok ? slot : 0;
+    if (p.cg.token_major) {
+      kk.code_off = sl * (kD + 4);
+      kk.scale_off = kk.code_off + kD;
+    } else {
+      long long page, off;
+      slot_page(p.cg, sl, page, off);
+      kk.code_off = page * p.cg.page_bytes + off * kD;
+      kk.scale_off = page * p.cg.page_bytes + static_cast<long long>(p.cg.page_size) * kD + 4 * off;
+    }
+    const bool real = k0 + 32LL * b + lane < k1;
+    kk.store = real && pos_ok && slot_ok;
+    kk.err = !real || (pos_ok && slot_ok) ? 0 : pos_ok ? DSA_DEVERR_SLOT : DSA_DEVERR_POSITION;
+    keys[32 * (b & 1) + lane] = kk;
+  };
+  long long pos0 = 0, slot0 = 0, nb_pos = 0, nb_slot = 0;
+  if (n > 0) {  // the loads go out now; resolving batch 0 waits for them
+    batch(0, pos0, slot0);
     batch(1, nb_pos, nb_slot);
   }
   // Copy step j into its stage, as two cp.async groups (empty past the warp's
   // last step).  Rows: for each of the step's keys u = 4h + q, lane l of
   // quarter-warp q copies bytes 16l and 128 + 16l of the key row.  Rotation:
-  // each lane copies its own cos/sin values of the key, and lane 0 stores the
-  // key's slot and position check.  The rows need no position, so the first
-  // step's rows go out before the first batch of positions has arrived.
+  // each lane copies its own cos/sin values of the key.  The rows need no
+  // position, so the first step's rows go out before the first batch of
+  // positions has arrived.
   auto issue_rows = [&](int j) {
     if (j < n) {
       const uint32_t st = ring + (j % kStreamStages) * SS::BYTES;
@@ -472,29 +512,20 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
   };
   auto issue_rot = [&](int j) {
     if (j < n) {
-      if (j > 0 && j % SPB == 0) {  // the next batch of 32 keys
-        b_pos = nb_pos;
-        b_slot = nb_slot;
+      if (j > 0 && j % SPB == 0) {  // the next batch of 32 keys becomes current
+        resolve(j / SPB, nb_pos, nb_slot);
+        __syncwarp();
         batch(j / SPB + 1, nb_pos, nb_slot);
       }
-      const uint32_t st = ring + (j % kStreamStages) * SS::BYTES;
-      unsigned char* st_p = ring_p + (j % kStreamStages) * SS::BYTES;
+      if constexpr (RP > 0) {
+        const uint32_t st = ring + (j % kStreamStages) * SS::BYTES;
+        const StreamKey* kb = keys + 32 * ((j / SPB) & 1) + kStreamKeys * (j % SPB);
 #pragma unroll
-      for (int h = 0; h < kStreamKPQ; ++h) {
-        const int u = 4 * h + qtr;
-        const int src = kStreamKeys * (j % SPB) + u;
-        const long long pos = __shfl_sync(kFull, b_pos, src);
-        const long long slot = __shfl_sync(kFull, b_slot, src);
-        const bool pos_ok = pos >= 0 && pos < p.max_pos;
-        if constexpr (RP > 0) {
-          const long long crow = (pos_ok ? pos : 0) * p.cs_stride + RP * l;
+        for (int h = 0; h < kStreamKPQ; ++h) {
+          const int u = 4 * h + qtr;
+          const long long crow = kb[u].cs_off + RP * l;
           cp_async_rot<RP>(st + SS::COS + SS::CS * u + 4 * RP * l, p.cos_t + crow);
           cp_async_rot<RP>(st + SS::SIN + SS::CS * u + 4 * RP * l, p.sin_t + crow);
-        }
-        if (l == 0) {
-          long long* idx = reinterpret_cast<long long*>(st_p + SS::IDX + 16 * u);
-          idx[0] = slot;
-          idx[1] = pos_ok ? 1 : 0;
         }
       }
     }
@@ -504,7 +535,11 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
   // Groups in commit order: rows(0), rot(0), rows(1), rot(1), ...; with step
   // j + 1 in flight, step j has landed once at most two groups are pending.
   static_assert(kStreamStages == 2, "the wait counts below assume two stages");
-  issue_rows(0);
+  issue_rows(0);  // before the first positions are needed
+  if (n > 0) {
+    resolve(0, pos0, slot0);
+    __syncwarp();
+  }
   issue_rot(0);
   for (int j = 0; j < n; ++j) {
     // refill the stage freed by step j - 1, then wait for step j
@@ -513,18 +548,20 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
     cp_async_wait<2>();
     __syncwarp();
     const uint32_t st = ring + (j % kStreamStages) * SS::BYTES;
-    const unsigned char* st_p = ring_p + (j % kStreamStages) * SS::BYTES;
+    const StreamKey* kb = keys + 32 * ((j / SPB) & 1) + kStreamKeys * (j % SPB);
     float x[kStreamKPQ][16];
     Rot<RP> r[kStreamKPQ];
-    bool real[kStreamKPQ], pos_ok[kStreamKPQ];
-    long long slot[kStreamKPQ];
+    uint8_t* code[kStreamKPQ];
+    float* scale[kStreamKPQ];
+    bool store[kStreamKPQ];
+    int err[kStreamKPQ];
 #pragma unroll
     for (int h = 0; h < kStreamKPQ; ++h) {
       const int u = 4 * h + qtr;
-      const long long* idx = reinterpret_cast<const long long*>(st_p + SS::IDX + 16 * u);
-      slot[h] = idx[0];
-      pos_ok[h] = idx[1] != 0;
-      real[h] = k0 + static_cast<long long>(kStreamKeys) * j + u < k1;
+      code[h] = p.cg.cache + kb[u].code_off;
+      scale[h] = reinterpret_cast<float*>(p.cg.cache + kb[u].scale_off);
+      store[h] = kb[u].store != 0;
+      err[h] = kb[u].err;
       load_vec<HAD, STYLE, RP, SharedMem>(st + SS::ROW * u, l, x[h]);
       if constexpr (RP > 0) {
         load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(st + SS::COS + SS::CS * u + 4 * RP * l, r[h].c);
@@ -532,7 +569,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
         finish_rot<RP>(r[h]);
       }
     }
-    k_multi<HAD, STYLE, RP, kStreamKPQ>(p, x, r, l, real, pos_ok, slot);
+    k_multi<HAD, STYLE, RP, kStreamKPQ>(p, x, r, l, code, scale, store, err);
     __syncwarp();  // every lane is done with this stage before it is refilled
   }
 }
