@@ -71,6 +71,10 @@ TRAFFIC_JSON = {"prefill": os.path.join(ROOT, "profiles", "traffic_prefill_T8192
                 "k_only": os.path.join(ROOT, "profiles", "traffic_k_only_T65536.json")}
 TRAFFIC_KERNEL = {"prefill": "dsa_pipeline_kernel", "decode": "dsa_direct_kernel",
                   "k_only": "dsa_kstream_kernel"}
+# The decode probe repeats one small input set, which stays in L2 between
+# launches; its capture flushes the caches before each launch instead, so
+# the inputs come from DRAM (and the outputs stay in L2 within the window).
+TRAFFIC_CACHE = {"prefill": "none", "decode": "all", "k_only": "none"}
 TRAFFIC_METRICS = ("dram__bytes_read.sum,dram__bytes_write.sum,lts__t_sectors_op_write.sum,"
                    "lts__t_sectors_op_read.sum,gpu__time_duration.sum")
 KERNEL_SRCS = [os.path.join(ROOT, "prep_token_gb300", "csrc", f)
@@ -133,9 +137,11 @@ def profile_traffic(which="prefill"):
 
 def write_traffic_json(csv_path, which):
     """Turn an ncu --csv launch list of the TRAFFIC_METRICS (two back-to-back
-    launches of one kernel, --cache-control none) into the committed summary:
-    the figures of the last launch, which also drains what the one before
-    left dirty in L2, so its DRAM writes are those of a launch in a stream."""
+    launches of one kernel) into the committed summary: the figures of the
+    last launch.  With --cache-control none (prefill, k-only: inputs larger
+    than L2) that launch also drains what the one before left dirty in L2,
+    so its DRAM writes are those of a launch in a stream; the decode capture
+    flushes the caches before each launch (TRAFFIC_CACHE)."""
     import csv
     launches = {}
     name = None
@@ -156,7 +162,8 @@ def write_traffic_json(csv_path, which):
         "workload": {"prefill": "prefill T=8192 H=64 NeoX (synth.make_prefill(seed=3))",
                      "decode": "decode T=64 H=64 GPT-J (synth.make_decode(seed=1))",
                      "k_only": "k-only T=65536 (synth.make_k_bulk, four input sets cycled)"}[which],
-        "command": (f"ncu --metrics {TRAFFIC_METRICS} --cache-control none --clock-control none "
+        "command": (f"ncu --metrics {TRAFFIC_METRICS} --cache-control {TRAFFIC_CACHE[which]} "
+                    f"--clock-control none "
                     f"-k regex:{TRAFFIC_KERNEL[which]} -s 2 -c 2 --csv --log-file traffic.csv "
                     f"python bench.py --probe {probe}"),
         "launches_captured": len(launches),
