@@ -440,50 +440,58 @@ def _k_bulk_timing(dp, torch, dev, peaks, reps=20, n_sets=4):
     """The k-only call at prefill size (65,536 keys, 8 sequences of 8192),
     both pairings: us per call over a graph of 8 calls that cycles through
     `n_sets` input sets (k|w rows, slots and caches; 4 x 43 MB, more than the
-    129 MB L2), so every call reads its keys from HBM."""
+    129 MB L2), so every call reads its keys from HBM.  Plain launches, PDL
+    launches, and PDL with the positions and cos/sin read before the wait
+    (pdl="early": the k rows come from the previous kernel, the rest not)."""
     import synth
     out = {}
+    kbytes = None
     for style, name in ((synth.NEOX, "neox"), (synth.GPTJ, "gptj")):
         sets = []
         for i in range(n_sets):
             inp = synth.make_k_bulk(seed=6 + i, style=style)
             sets.append((inp, _k_dev_inputs(inp, dev)))
         stream = torch.cuda.Stream(device=dev)
+        T = sets[0][0].T
+        kbytes = synth.algorithmic_bytes(T, 0, with_q=False)
 
-        def call(inp, d):
+        def call(inp, d, pdl):
             dp.dsa_indexer_k_prepare_store(
                 d["k"], d["positions"], d["slots"], d["cos"], d["sin"], d["gamma"], d["beta"],
                 inp.eps, d["cache"], inp.page_size, inp.rope_dim, inp.style,
-                max_position=inp.max_position, stream=stream)
+                max_position=inp.max_position, pdl=pdl, stream=stream)
 
-        with torch.cuda.stream(stream):
-            for inp, d in sets:
-                call(inp, d)
-        stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(8):
-                call(*sets[i % n_sets])
-        with torch.cuda.stream(stream):
-            g.replay()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(reps):
+        def timed(pdl):
+            with torch.cuda.stream(stream):
+                for inp, d in sets:
+                    call(inp, d, pdl)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(8):
+                    call(*sets[i % n_sets], pdl)
+            with torch.cuda.stream(stream):
                 g.replay()
-            e1.record(stream)
-        stream.synchronize()
-        del g
-        T = sets[0][0].T
-        us = e0.elapsed_time(e1) * 1000.0 / (8 * reps)
-        kbytes = synth.algorithmic_bytes(T, 0, with_q=False)
-        out[name] = {"us_per_call": us, "calls": 8 * reps, "gb_per_s": kbytes / (us * 1e-6) / 1e9,
-                     "hbm_frac": kbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
-                     "keys_per_s": T / (us * 1e-6)}
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            stream.synchronize()
+            del g
+            us = e0.elapsed_time(e1) * 1000.0 / (8 * reps)
+            gbs = kbytes / (us * 1e-6) / 1e9
+            return {"us_per_call": us, "calls": 8 * reps, "gb_per_s": gbs,
+                    "hbm_frac": gbs / peaks["hbm_gbs"], "keys_per_s": T / (us * 1e-6)}
+
+        out[name] = timed(False)
+        out[name]["pdl"] = timed(True)
+        out[name]["pdl_early"] = timed("early")
         out["workload"] = (f"k-only T={T} (8 x 8192 tokens) rope_dim=64, 2048 shuffled pages, "
                            f"{n_sets} input sets cycled (larger than L2)")
-        out["algorithmic_bytes"] = kbytes
         del sets
+    out["algorithmic_bytes"] = kbytes
     return out
 
 

@@ -225,10 +225,18 @@ __device__ __forceinline__ void k_multi(const Params& p, float (&x)[N][16], cons
 #pragma unroll
   for (int n = 0; n < N; ++n) {
     if (err[n] && l == 0) raise_error(p, err[n]);
-    if constexpr (HAD)
-      store_hslice<STYLE, RP, 4>(code[n], l, wa[n], store[n]);
-    else
-      store_slice<STYLE, RP, 4>(code[n], l, wa[n], wb[n], wp[n], store[n]);
+    // paged rows start on 16 bytes, token-major ones (132 bytes apart) on 4
+    if (p.cg.token_major) {
+      if constexpr (HAD)
+        store_hslice<STYLE, RP, 4>(code[n], l, wa[n], store[n]);
+      else
+        store_slice<STYLE, RP, 4>(code[n], l, wa[n], wb[n], wp[n], store[n]);
+    } else {
+      if constexpr (HAD)
+        store_hslice<STYLE, RP>(code[n], l, wa[n], store[n]);
+      else
+        store_slice<STYLE, RP>(code[n], l, wa[n], wb[n], wp[n], store[n]);
+    }
     store_f32(scale[n], pow2f(e[n]), store[n] && l == 0);
   }
 }
@@ -451,7 +459,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
   const long long k1 = min(static_cast<long long>(p.T), kStreamKeys * ((w + 1) * steps / nw));
   const int n = k0 < k1 ? static_cast<int>((k1 - k0 + kStreamKeys - 1) / kStreamKeys) : 0;
   grid_launch_dependents();
-  grid_dependency_wait();
+  if (!p.early_rope) grid_dependency_wait();
   unsigned char* const wbase = smem + wi * kstream_warp_bytes<RP>();
   const uint32_t ring = smem_u32(wbase);
   StreamKey* const keys = reinterpret_cast<StreamKey*>(wbase + kStreamStages * SS::BYTES);
@@ -532,15 +540,29 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
     cp_async_commit();
   };
 
-  // Groups in commit order: rows(0), rot(0), rows(1), rot(1), ...; with step
-  // j + 1 in flight, step j has landed once at most two groups are pending.
+  // Groups in commit order: rows(0) and rot(0) (either first), rows(1),
+  // rot(1), ...; with step j + 1 in flight, step j has landed once at most two
+  // groups are pending.
   static_assert(kStreamStages == 2, "the wait counts below assume two stages");
-  issue_rows(0);  // before the first positions are needed
-  if (n > 0) {
-    resolve(0, pos0, slot0);
-    __syncwarp();
+  if (p.early_rope) {
+    // DSA_FLAG_PDL_EARLY_ROPE: positions, slots and the cos/sin cache are not
+    // the previous kernel's outputs, so the first cos/sin rows are on their
+    // way before the wait; only the key rows wait for it.
+    if (n > 0) {
+      resolve(0, pos0, slot0);
+      __syncwarp();
+    }
+    issue_rot(0);
+    grid_dependency_wait();
+    issue_rows(0);
+  } else {
+    issue_rows(0);  // before the first positions are needed
+    if (n > 0) {
+      resolve(0, pos0, slot0);
+      __syncwarp();
+    }
+    issue_rot(0);
   }
-  issue_rot(0);
   for (int j = 0; j < n; ++j) {
     // refill the stage freed by step j - 1, then wait for step j
     issue_rows(j + 1);

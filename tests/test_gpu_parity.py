@@ -280,6 +280,25 @@ def test_pdl_launch_matches():
     assert np.array_equal(k_cache.cpu().numpy(), plain["cache"])
 
 
+@pytest.mark.parametrize("n_seq,seq_len,style", [(2, 5120, synth.NEOX), (2, 5120, synth.GPTJ),
+                                                  (8, 8192, synth.NEOX)])
+def test_k_stream_bulk_and_pdl_modes(n_seq, seq_len, style):
+    """The k-only call at prefill size takes the k-stream kernel (more than
+    8192 keys): against the oracle on every key, at the bench's 65,536 keys
+    too, and with the same bytes under PDL and with its first positions and
+    cos/sin rows read before the PDL wait (pdl="early")."""
+    inp = synth.make_k_bulk(seed=31, style=style, n_seq=n_seq, seq_len=seq_len,
+                            pages=max(200, n_seq * seq_len // 64))
+    d = to_device(inp)
+    plain = run_k(inp, d)
+    assert_parity(inp, plain, run_oracle_k(inp))
+    for mode in (True, "early"):
+        got = run_k(inp, d, pdl=mode)
+        assert np.array_equal(got["cache"], plain["cache"]), mode
+    direct = run_k(inp, d, kernel="direct")
+    assert np.array_equal(direct["cache"], plain["cache"])
+
+
 def test_head_stride_not_contiguous_uses_per_head_copies():
     """q rows that are not packed head after head (sq_h != 128) take one copy
     per head; the bytes must not change."""
