@@ -455,8 +455,16 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
   const long long nw = static_cast<long long>(gridDim.x) * kStreamWarps;
   const long long steps = (static_cast<long long>(p.T) + kStreamKeys - 1) / kStreamKeys;
   const long long w = static_cast<long long>(blockIdx.x) * kStreamWarps + wi;
-  const long long k0 = kStreamKeys * (w * steps / nw);
-  const long long k1 = min(static_cast<long long>(p.T), kStreamKeys * ((w + 1) * steps / nw));
+  long long s0, s1;  // (32-bit divisions while the products fit: shorter)
+  if ((w + 1) * steps <= 0xffffffffLL) {
+    s0 = static_cast<uint32_t>(w * steps) / static_cast<uint32_t>(nw);
+    s1 = static_cast<uint32_t>((w + 1) * steps) / static_cast<uint32_t>(nw);
+  } else {
+    s0 = w * steps / nw;
+    s1 = (w + 1) * steps / nw;
+  }
+  const long long k0 = kStreamKeys * s0;
+  const long long k1 = min(static_cast<long long>(p.T), kStreamKeys * s1);
   const int n = k0 < k1 ? static_cast<int>((k1 - k0 + kStreamKeys - 1) / kStreamKeys) : 0;
   grid_launch_dependents();
   if (!p.early_rope) grid_dependency_wait();
@@ -542,7 +550,8 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
 
   // Groups in commit order: rows(0) and rot(0) (either first), rows(1),
   // rot(1), ...; with step j + 1 in flight, step j has landed once at most two
-  // groups are pending.
+  // groups are pending.  (Issuing rows(1) before the first positions have
+  // arrived measured slower: it delays the chain to the first cos/sin rows.)
   static_assert(kStreamStages == 2, "the wait counts below assume two stages");
   if (p.early_rope) {
     // DSA_FLAG_PDL_EARLY_ROPE: positions, slots and the cos/sin cache are not
