@@ -1012,4 +1012,60 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// ---------------------------------------------------------------- staged LayerNorm parameters
+//
+// Element index of register r of lane l: the balanced slice, or the
+// Hadamard layout.
+template <bool HAD, int STYLE, int RP>
+__device__ __forceinline__ int slice_elem(int l, int r) {
+  if constexpr (HAD) {
+    using S = HSlice<STYLE, RP>;
+    return S::off(r) + S::W * l;
+  } else {
+    using S = Slice<STYLE, RP>;
+    if (r >= 2 * RP) return S::P_BASE + S::NP * l + (r - 2 * RP);
+    if (S::NEOX) return r < RP ? RP * l + r : S::B_BASE + RP * l + (r - RP);
+    return 2 * RP * l + (r < RP ? 2 * r : 2 * (r - RP) + 1);
+  }
+}
+
+// gamma and beta staged in shared memory in the lanes' register order, so
+// that the affine step reads four registers' worth at once and runs packed in
+// every layout: gamma's registers 4k .. 4k+3 of lane l at byte 16 (8k + l)
+// (a quarter-warp's eight lanes read 128 contiguous bytes), beta 512 bytes on.
+constexpr int kStagedGbBytes = 2 * 4 * kD;
+
+// Thread `i` (0 .. 255) of a block stages value i of the layout above.
+template <bool HAD, int STYLE, int RP>
+__device__ __forceinline__ void stage_gb(float* dst, const float* gamma, const float* beta, int i) {
+  const int j = i & 127;
+  const int r = 4 * (j >> 5) + (j & 3);
+  const int l = (j >> 2) & 7;
+  dst[i] = __ldg((i < 128 ? gamma : beta) + slice_elem<HAD, STYLE, RP>(l, r));
+}
+
+// y = x * rstd * gamma + beta for M vectors of lane l, from the staged rows
+// at shared byte address gb; each piece is read once for all M.
+template <int M>
+__device__ __forceinline__ void affine_staged(uint32_t gb, int l, float (&x)[M][16],
+                                              const float (&rstd)[M]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float g[4], b[4];
+    load_f32_shared<4, 16>(gb + 16 * (8 * k + l), g);
+    load_f32_shared<4, 16>(gb + 4 * kD + 16 * (8 * k + l), b);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      const float2 r2 = make_float2(rstd[m], rstd[m]);
+#pragma unroll
+      for (int i = 0; i < 4; i += 2) {
+        const float2 y = __ffma2_rn(__fmul2_rn(make_float2(x[m][4 * k + i], x[m][4 * k + i + 1]), r2),
+                                    make_float2(g[i], g[i + 1]), make_float2(b[i], b[i + 1]));
+        x[m][4 * k + i] = y.x;
+        x[m][4 * k + i + 1] = y.y;
+      }
+    }
+  }
+}
+
 }  // namespace dsa_dev

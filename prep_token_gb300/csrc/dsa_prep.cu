@@ -196,7 +196,11 @@ cudaError_t launch(Params& p, int rope_style, uint32_t flags, bool w_rows_aligne
         !(flags & DSA_FLAG_DIRECT) && ((flags & DSA_FLAG_PIPELINE) || p.T > kStreamMinKeys);
     if (stream_k) {
       const long long steps = (static_cast<long long>(p.T) + kStreamKeys - 1) / kStreamKeys;
-      long long blocks = static_cast<long long>(sms) * kStreamCtas;
+      // as many CTAs as are resident at once (one per SM at rope_dim 128,
+      // whose ring takes more than half of an SM's shared memory)
+      int per_sm = kStreamCtas;
+      while (per_sm > 1 && per_sm * (kStreamSmem[ri] + 1024) > smem_per_sm) --per_sm;
+      long long blocks = static_cast<long long>(sms) * per_sm;
       const long long need = (steps + kStreamWarps - 1) / kStreamWarps;
       if (blocks > need) blocks = need;
       cfg.gridDim = dim3(static_cast<unsigned>(blocks));

@@ -190,7 +190,7 @@ __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const R
 }
 
 // Several keys at once, N per quarter-warp: the steps of k_slice with gamma
-// and beta read piece by piece from global memory (k_slice<..., false>), each
+// and beta read from their staged copy in shared memory (stage_gb), each
 // phase run for all N keys before the next so their dependent chains
 // interleave, and each gamma/beta piece loaded once for all N.  Per key the
 // arithmetic is k_slice's, so the bytes written are the same.  The caller
@@ -200,14 +200,11 @@ __device__ __forceinline__ void k_slice(const Params& p, float (&x)[16], const R
 template <bool HAD, int STYLE, int RP, int N>
 __device__ __forceinline__ void k_multi(const Params& p, float (&x)[N][16], const Rot<RP> (&r)[N],
                                         int l, uint8_t* const (&code)[N], float* const (&scale)[N],
-                                        const bool (&store)[N], const int (&err)[N]) {
+                                        const bool (&store)[N], const int (&err)[N], uint32_t gb) {
   float rstd[N];
 #pragma unroll
   for (int n = 0; n < N; ++n) rstd[n] = ln_center(x[n], p.eps);
-  if constexpr (HAD)
-    affine_hslice<STYLE, RP, N>(p.gamma, p.beta, l, x, rstd);
-  else
-    affine_slice<STYLE, RP, N>(p.gamma, p.beta, l, x, rstd);
+  affine_staged<N>(gb, l, x, rstd);
   int e[N];
   uint32_t wa[N][4], wb[N][4], wp[N][4];
 #pragma unroll
@@ -381,13 +378,16 @@ __global__ void __launch_bounds__(kDirectThreads) dsa_direct_kernel(const Params
 // into a per-warp table in shared memory (two batches deep), so no lane
 // repeats that scalar work for its key.  Every input of a step -- the key
 // rows and their cos/sin row slices -- is copied by cp.async into a stage of
-// the warp's shared-memory ring kStreamStages - 1 steps ahead of the math.
-// Per key the arithmetic is that of the other kernels, so every kernel
-// writes the same bytes.
+// the warp's shared-memory ring kStreamStages - 1 steps ahead of the math;
+// gamma and beta are staged once per CTA, in the lanes' register order
+// (stage_gb), so the affine step runs packed in every layout.  Per key the
+// arithmetic is that of the other kernels, so every kernel writes the same
+// bytes.
 constexpr int kStreamKPQ = 2;                 // keys per quarter-warp per step
 constexpr int kStreamKeys = 4 * kStreamKPQ;   // keys per warp per step
 constexpr int kStreamWarps = 8;
 constexpr int kStreamThreads = 32 * kStreamWarps;
+static_assert(kStreamThreads == 2 * kD, "stage_gb: one gamma or beta value a thread");
 constexpr int kStreamStages = 2;              // the step computed and the one in flight
 constexpr int kStreamCtas = 2;                // resident CTAs per SM the grid is sized for
 
@@ -423,7 +423,7 @@ __host__ __device__ constexpr int kstream_warp_bytes() {
 
 template <int RP>
 __host__ __device__ constexpr int kstream_smem() {
-  return kStreamWarps * kstream_warp_bytes<RP>();
+  return kStagedGbBytes + kStreamWarps * kstream_warp_bytes<RP>();
 }
 
 // cp.async of the lane's RP fp32 values (4 * RP bytes, aligned to that or 16).
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
   const int n = k0 < k1 ? static_cast<int>((k1 - k0 + kStreamKeys - 1) / kStreamKeys) : 0;
   grid_launch_dependents();
   if (!p.early_rope) grid_dependency_wait();
-  unsigned char* const wbase = smem + wi * kstream_warp_bytes<RP>();
+  unsigned char* const wbase = smem + kStagedGbBytes + wi * kstream_warp_bytes<RP>();
   const uint32_t ring = smem_u32(wbase);
   StreamKey* const keys = reinterpret_cast<StreamKey*>(wbase + kStreamStages * SS::BYTES);
 
@@ -572,6 +572,9 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
     }
     issue_rot(0);
   }
+  // gamma and beta, once per CTA, in the lanes' register order
+  stage_gb<HAD, STYLE, RP>(reinterpret_cast<float*>(smem), p.gamma, p.beta, threadIdx.x);
+  __syncthreads();
   for (int j = 0; j < n; ++j) {
     // refill the stage freed by step j - 1, then wait for step j
     issue_rows(j + 1);
@@ -600,7 +603,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) dsa_kstream_kerne
         finish_rot<RP>(r[h]);
       }
     }
-    k_multi<HAD, STYLE, RP, kStreamKPQ>(p, x, r, l, code, scale, store, err);
+    k_multi<HAD, STYLE, RP, kStreamKPQ>(p, x, r, l, code, scale, store, err, smem_u32(smem));
     __syncwarp();  // every lane is done with this stage before it is refilled
   }
 }
