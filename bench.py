@@ -1002,6 +1002,21 @@ def _logits_timing(dp, torch, dev, peaks, calls=10, reps=20):
             "gpu_launches": calls * reps}
 
 
+def probe_workload(which):
+    """The inputs and the Hadamard switch of a q+k probe: prefill, prefill_h32,
+    prefill_h16, decode, prefill_hadamard or decode_hadamard."""
+    import synth
+    had = which.endswith("_hadamard")
+    base = which[:-len("_hadamard")] if had else which
+    if base == "decode":
+        return synth.make_decode(seed=1), had
+    if base == "prefill":
+        return synth.make_prefill(seed=3), had
+    if base.startswith("prefill_h") and base[len("prefill_h"):].isdigit():
+        return synth.make_prefill(seed=3, H=int(base[len("prefill_h"):])), had
+    raise ValueError(f"no probe workload {which!r}")
+
+
 def run_probe(which, local_rank):
     """A few eager calls on one workload, for ncu captures (no timing, no JSON)."""
     import torch
@@ -1028,13 +1043,7 @@ def run_probe(which, local_rank):
         torch.cuda.synchronize(dev)
         print(f"probe k_only: 6 calls (T={inp.T}, four input sets)")
         return
-    had = which.endswith("_hadamard")
-    if which.startswith("decode"):
-        inp = synth.make_decode(seed=1)
-    elif which.startswith("prefill_h"):
-        inp = synth.make_prefill(seed=3, H=int(which[len("prefill_h"):]))
-    else:
-        inp = synth.make_prefill(seed=3)
+    inp, had = probe_workload(which)
     d = _dev_inputs(inp, dev)
     stream = torch.cuda.current_stream()
     for _ in range(6):

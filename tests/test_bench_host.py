@@ -42,3 +42,17 @@ def test_traffic_summary_round_trip(tmp_path, monkeypatch):
     stale["kernel_source_sha256"] = "0" * 64
     out.write_text(json.dumps(stale))
     assert bench.profile_traffic("prefill") is None
+
+
+def test_probe_workloads():
+    """Every q+k probe that ncu captures use names its own workload (the
+    Hadamard probes the plain shapes with the rotation on)."""
+    import bench
+    for which, T, H, had in [("prefill", 8192, 64, False), ("prefill_h32", 8192, 32, False),
+                             ("prefill_h16", 8192, 16, False), ("decode", 64, 64, False),
+                             ("prefill_hadamard", 8192, 64, True), ("decode_hadamard", 64, 64, True)]:
+        inp, h = bench.probe_workload(which)
+        assert (inp.T, inp.H, h) == (T, H, had), which
+    import pytest
+    with pytest.raises(ValueError):
+        bench.probe_workload("prefill_hx")
