@@ -145,11 +145,15 @@ def test_two_writer_statistic(golden_dir):
     d = code_distance(codes_f[rows], codes_u[rows])
     assert d.max() <= note["max_code_distance"]
     frac = (d > 0).mean()
-    # A bf16 rounding changes the E4M3 code only for values within half a bf16
-    # step (2^-8 of the binade) of an E4M3 midpoint (steps of 2^-3) whose tie
-    # goes the other way: about 1/32 of elements.  The pages saw 15 / 5248 on
-    # model data; here the rate is bounded by the window estimate.
-    assert 0 < frac <= 1.5 / 32, (frac, page_frac)
+    # The unfused chain rounds each element to bf16 twice (the LayerNorm
+    # output, then the rotated vector).  A rounding error is uniform within
+    # half a bf16 step, 2^-8 of the binade, so its mean size is 2^-9 of the
+    # binade; E4M3 midpoints are 2^-3 apart, so one rounding crosses one with
+    # probability 2^-9 / 2^-3 = 1/64, and two about 1/32 (the scale exponent
+    # shifts both grids alike).  The measured rate must sit at that estimate
+    # (1.00/32 on this seed and its neighbours); the pages saw 15 / 5248 on
+    # model data, whose values are not uniform within a binade.
+    assert 0.75 / 32 <= frac <= 1.25 / 32, (frac, page_frac)
     # fused is closer to the float64 truth on most differing elements
     from _brute import bf16, rope64
     dec = oracle.e4m3_decode(np.arange(256, dtype=np.uint8)).astype(np.float64)
