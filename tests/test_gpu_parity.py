@@ -155,7 +155,11 @@ def test_live_token_slice():
     assert torch.all(q_out[40:] == 0x5A) and torch.all(w_out[40:] == -7.0)
 
 
-def test_device_error_bits():
+@pytest.mark.parametrize("kernel", ["direct", "pipeline"])
+def test_device_error_bits(kernel):
+    """Bad positions and slots set their error bits and write nothing, in
+    every kernel (k-only with kernel="pipeline" is the k-stream kernel), and
+    the other tokens still match the oracle."""
     inp = synth.make_decode(seed=12, T=20, H=4)
     inp.positions = inp.positions.copy()
     inp.slots = inp.slots.copy()
@@ -165,7 +169,7 @@ def test_device_error_bits():
     inp.slots[9] = -5
     d = to_device(inp)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    gpu = run_qk(inp, d, err=err)
+    gpu = run_qk(inp, d, err=err, kernel=kernel)
     ref = run_oracle_qk(inp)
     assert ref["err"] == 3 and int(err.item()) == 3
     ok = np.ones(inp.T, bool)
@@ -176,11 +180,13 @@ def test_device_error_bits():
                   dict(q_fp8=ref["q_fp8"][ok], weights=ref["weights"][ok], cache=ref["cache"]))
     assert rep["ok"], rep
     err.zero_()
-    run_k(inp, d, err=err)
+    gk = run_k(inp, d, err=err, kernel=kernel)
     assert int(err.item()) == 3
+    assert np.array_equal(gk["cache"], gpu["cache"])
     err.zero_()
     good = synth.make_decode(seed=12, T=20, H=4)
-    run_qk(good, to_device(good), err=err)
+    run_qk(good, to_device(good), err=err, kernel=kernel)
+    run_k(good, to_device(good), err=err, kernel=kernel)
     assert int(err.item()) == 0
 
 
@@ -297,6 +303,23 @@ def test_k_stream_bulk_and_pdl_modes(n_seq, seq_len, style):
         assert np.array_equal(got["cache"], plain["cache"]), mode
     direct = run_k(inp, d, kernel="direct")
     assert np.array_equal(direct["cache"], plain["cache"])
+
+
+def test_k_stream_error_bits():
+    """Bad positions and slots spread over many batches of the k-stream
+    kernel's key table: their error bits are set, they write nothing, and
+    every other key matches the oracle."""
+    inp = synth.make_k_bulk(seed=33, n_seq=2, seq_len=5120, pages=200)
+    inp.positions = inp.positions.copy()
+    inp.slots = inp.slots.copy()
+    inp.positions[[5, 4099]] = [-3, inp.max_position]
+    inp.slots[[31, 32, 10239]] = [inp.num_pages * inp.page_size, -1, -64]
+    d = to_device(inp)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_k(inp, d, err=err)
+    ref = run_oracle_k(inp)
+    assert ref["err"] == 3 and int(err.item()) == 3
+    assert_parity(inp, got, ref)
 
 
 def test_head_stride_not_contiguous_uses_per_head_copies():
