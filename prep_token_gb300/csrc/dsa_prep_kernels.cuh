@@ -23,18 +23,22 @@
 // needs no shuffles, and it runs as packed f32x2 FMUL2/FFMA2.  A warp
 // handles four vectors per instruction stream.
 //
-// Two kernels share that math:
+// Three kernels share that math:
 //   * dsa_pipeline_kernel (large calls): persistent, warp-specialised.  Warp 0
 //     moves each unit -- one token and up to 64 of its heads, plus the key on
-//     the first chunk -- from HBM into a 4-stage shared-memory ring with
-//     cp.async.bulk copies counted on mbarriers; 8 consumer warps compute from
-//     shared memory and store to HBM.  Bytes in flight are set by the ring
-//     (up to ~200 KB per SM), not by registers.
+//     the first chunk, or several whole tokens when they have few heads --
+//     from HBM into a 4-stage shared-memory ring with cp.async.bulk copies
+//     counted on mbarriers; 8 consumer warps compute from shared memory and
+//     store to HBM.  Bytes in flight are set by the ring (up to ~200 KB per
+//     SM), not by registers.
 //   * dsa_direct_kernel (small calls, decode): one warp per four vectors,
 //     every input in flight at once in two cp.async groups (the position and
 //     slot first, so the cos/sin loads go out while the rows still travel),
 //     warps spread over the SMs; the least latency per call.
-// Both come in a Hadamard variant (HAD = true) that rotates every vector by
+//   * dsa_kstream_kernel (large k-only calls): persistent warps over
+//     contiguous key ranges, two keys per quarter-warp, a cp.async ring per
+//     warp one step ahead of the math.
+// All come in a Hadamard variant (HAD = true) that rotates every vector by
 // H_128 / sqrt(128) after RoPE; it uses the HSlice lane layout.
 // Every mbarrier wait is bounded in time (DSA_DEVERR_TIMEOUT); nothing traps.
 #pragma once
