@@ -102,6 +102,16 @@ def test_decode_full_size_all_tokens():
     print("max err/tol", worst)
 
 
+def test_decode_full_size_ragged():
+    """The same step with context lengths uniform in [1, 16384]: each token's
+    tiles end at its own length (the last one part-filled), every column
+    beyond it is -inf, and the CTAs of short tokens have no tiles at all."""
+    li = synth.make_logits(seed=11, T=64, H=64, context=16384, ragged=True)
+    assert li.context_lens.min() < 4096 and li.max_context > 12288
+    worst = _check(li)
+    print("max err/tol", worst)
+
+
 def test_bad_page_sets_error_bit_and_nan_columns():
     """A block-table entry outside [0, num_pages) sets the error bit, and the
     64 columns of that block are NaN, as in the oracle; every other column
