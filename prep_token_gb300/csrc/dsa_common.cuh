@@ -508,13 +508,14 @@ __device__ __forceinline__ float ln_center(float (&x)[16], float eps) {
 // read straight off the exponent and fraction bits, no division or log.  The
 // compare rides a carry: fraction > 0x600000 exactly when fraction + 0x1fffff
 // reaches 2^23 and bumps the exponent field.
-__device__ __forceinline__ float vector_amax(const float (&x)[16]) {
+__device__ __forceinline__ float lane_amax(const float (&x)[16]) {
   float m = max3f(fabsf(x[0]), fabsf(x[1]), fabsf(x[2]));
 #pragma unroll
   for (int j = 3; j < 15; j += 2) m = max3f(m, fabsf(x[j]), fabsf(x[j + 1]));
-  m = fmaxf(m, fabsf(x[15]));
-  return quad_max(m);
+  return fmaxf(m, fabsf(x[15]));
 }
+
+__device__ __forceinline__ float vector_amax(const float (&x)[16]) { return quad_max(lane_amax(x)); }
 
 __device__ __forceinline__ int exponent_of_amax(float amax) {
   const uint32_t b = __float_as_uint(fmaxf(amax, 1e-4f));
@@ -1064,6 +1065,123 @@ __device__ __forceinline__ void affine_staged(uint32_t gb, int l, float (&x)[M][
         x[m][4 * k + i] = y.x;
         x[m][4 * k + i + 1] = y.y;
       }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- four-lane Hadamard layout
+//
+// The Hadamard variant's query path in the prefill kernel gives each vector
+// to four consecutive lanes: lane j of a group holds the HSlice slices of
+// lanes 2j and 2j + 1 of the eight-lane layout as two halves x0 and x1, in
+// those lanes' register order.  The butterfly stage on the eight-lane lane bit
+// 0 pairs the two halves inside the lane, the stages on lane bits 1 and 2 are
+// shuffles with the group's partners xor 1 and 2, the rest are register
+// stages: the same operations on the same values in the same stage order, so
+// the codes are those of the eight-lane layout, with a third fewer shuffles
+// and half the per-vector scalar work per lane.
+
+// The pair's bf16 row chunks (lane j of the group): eight-lane lanes 2j and
+// 2j + 1 own neighbouring W-element pieces of every chunk.
+template <int STYLE, int RP, class M>
+__device__ __forceinline__ void load_hslice_pair(typename M::Addr row, int j, float (&x0)[16],
+                                                 float (&x1)[16]) {
+  using S = HSlice<STYLE, RP>;
+#pragma unroll
+  for (int c = 0; c < S::NCH; ++c) {
+    float t[2 * S::W];
+    load_bf16<M, 2 * S::W, gcd_pow2(4 * S::W)>(row + 2 * (c * S::STRIDE + 2 * S::W * j), t);
+#pragma unroll
+    for (int i = 0; i < S::W; ++i) x0[S::reg(c, i)] = t[i], x1[S::reg(c, i)] = t[S::W + i];
+  }
+}
+
+// fwht_stage for the pair: B == W is the eight-lane lane bit 0 (the halves),
+// 2W and 4W the group partners xor 1 and 2.
+template <int STYLE, int RP, int H>
+__device__ __forceinline__ void fwht_stage_pair(float (&x0)[16], float (&x1)[16], int j) {
+  using S = HSlice<STYLE, RP>;
+  constexpr int B = 1 << H;
+  if constexpr (B == S::W) {
+#pragma unroll
+    for (int r = 0; r < 16; r += 2) {
+      const float2 a = make_float2(x0[r], x0[r + 1]);
+      const float2 b = make_float2(x1[r], x1[r + 1]);
+      const float2 sum = __fadd2_rn(a, b);
+      const float2 dif = __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);  // a - b, one rounding
+      x0[r] = sum.x, x0[r + 1] = sum.y;
+      x1[r] = dif.x, x1[r + 1] = dif.y;
+    }
+  } else if constexpr (B > S::W && B < S::STRIDE) {
+    constexpr int m = B / S::W / 2;
+    const float sg = (j & m) ? -1.0f : 1.0f;
+    const float2 sg2 = make_float2(sg, sg);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float (&x)[16] = h ? x1 : x0;
+#pragma unroll
+      for (int r = 0; r < 16; r += 2) {
+        const float2 y = make_float2(__shfl_xor_sync(kFull, x[r], m),
+                                     __shfl_xor_sync(kFull, x[r + 1], m));
+        const float2 t = __ffma2_rn(sg2, make_float2(x[r], x[r + 1]), y);
+        x[r] = t.x;
+        x[r + 1] = t.y;
+      }
+    }
+  } else {
+    fwht_local_pairs<STYLE, RP, B, 0>(x0);
+    fwht_local_pairs<STYLE, RP, B, 2>(x0);
+    fwht_local_pairs<STYLE, RP, B, 4>(x0);
+    fwht_local_pairs<STYLE, RP, B, 6>(x0);
+    fwht_local_pairs<STYLE, RP, B, 0>(x1);
+    fwht_local_pairs<STYLE, RP, B, 2>(x1);
+    fwht_local_pairs<STYLE, RP, B, 4>(x1);
+    fwht_local_pairs<STYLE, RP, B, 6>(x1);
+  }
+}
+
+template <int STYLE, int RP>
+__device__ __forceinline__ void fwht_pair(float (&x0)[16], float (&x1)[16], int j) {
+  fwht_stage_pair<STYLE, RP, 0>(x0, x1, j);
+  fwht_stage_pair<STYLE, RP, 1>(x0, x1, j);
+  fwht_stage_pair<STYLE, RP, 2>(x0, x1, j);
+  fwht_stage_pair<STYLE, RP, 3>(x0, x1, j);
+  fwht_stage_pair<STYLE, RP, 4>(x0, x1, j);
+  fwht_stage_pair<STYLE, RP, 5>(x0, x1, j);
+  fwht_stage_pair<STYLE, RP, 6>(x0, x1, j);
+}
+
+// amax of the pair's vector over the group of four lanes.
+__device__ __forceinline__ float pair_amax(const float (&x0)[16], const float (&x1)[16]) {
+  float m = fmaxf(lane_amax(x0), lane_amax(x1));
+  m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+  return fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+}
+
+// Store the pair's codes (quantize_hslice's words of each half) to a
+// 16-byte aligned 128-byte row: chunk c's two W-byte pieces are neighbours.
+template <int STYLE, int RP>
+__device__ __forceinline__ void store_hslice_pair(uint8_t* row, int j, const uint32_t (&w0)[4],
+                                                  const uint32_t (&w1)[4], bool pred) {
+  using S = HSlice<STYLE, RP>;
+  constexpr int A = gcd_pow2(2 * S::W);
+  uint32_t v[8];
+  if constexpr (S::W % 4 == 0) {
+#pragma unroll
+    for (int c = 0; c < S::NCH; ++c) {
+#pragma unroll
+      for (int i = 0; i < S::W / 4; ++i)
+        v[i] = w0[c * S::W / 4 + i], v[S::W / 4 + i] = w1[c * S::W / 4 + i];
+      store_codes<2 * S::W, A>(row + c * S::STRIDE + 2 * S::W * j, v, pred);
+    }
+  } else {
+    static_assert(S::W <= 2, "chunks of 1 or 2 codes");
+    constexpr uint32_t mask = (1u << (8 * S::W)) - 1u;
+#pragma unroll
+    for (int c = 0; c < S::NCH; ++c) {
+      const int sh = 8 * ((c * S::W) & 3);
+      v[0] = ((w0[(c * S::W) / 4] >> sh) & mask) | (((w1[(c * S::W) / 4] >> sh) & mask) << (8 * S::W));
+      store_codes<2 * S::W, A>(row + c * S::STRIDE + 2 * S::W * j, v, pred);
     }
   }
 }

@@ -622,7 +622,10 @@ constexpr int kPipeThreads = 32 * (1 + kConsumers);
 // Resident CTAs per SM the pipeline kernels are compiled for (registers per
 // thread <= 65536 / (kPipeThreads * this)); the launcher sizes grids to match.
 constexpr int kPipeCtas = 3;
-constexpr int kPipeCtasHad = 3;
+// The Hadamard variant's four-lane query path holds two slices a lane: it
+// runs spill-free at 2 CTAs per SM (up to 113 registers), which measured
+// faster than 3 with spills (48.5 against 53.3 us at T=8192, H=64).
+constexpr int kPipeCtasHad = 2;
 constexpr int kBarrierBytes = 128;  // full[kStages], empty[kStages], abort flag
 // stage layout of one-token units (byte offsets from the stage base)
 constexpr int kOffK = 64;      // key row, 256 B (after the StageHeader)
@@ -929,12 +932,17 @@ __device__ void consumer_single(const Params& p, int cw, unsigned char* ring, ui
     const int h0 = c * p.HC;
     const int n = min(p.HC, p.H - h0);
 
+    // the eight-lane rotation operands (the Hadamard variant's queries use
+    // their own, and its key loads these when it has one)
     Rot<RP> r;
-    if constexpr (RP > 0) {
-      load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(sts + kOffCos + 4 * RP * l, r.c);
-      load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(sts + kOffSin + 4 * RP * l, r.s);
-      finish_rot<RP>(r);
-    }
+    auto load_rot8 = [&]() {
+      if constexpr (RP > 0) {
+        load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(sts + kOffCos + 4 * RP * l, r.c);
+        load_f32_shared<RP, Slice<0, RP>::ALIGN_CS>(sts + kOffSin + 4 * RP * l, r.s);
+        finish_rot<RP>(r);
+      }
+    };
+    if constexpr (!HAD) load_rot8();
     // Per-unit bases, so a head costs a few 32-bit offsets: its output rows,
     // and its gate weights -- in the stage when they rode the bulk copy, else
     // in global memory; one generic pointer serves both.
@@ -954,13 +962,53 @@ __device__ void consumer_single(const Params& p, int cw, unsigned char* ring, ui
       const int e = q_slice<HAD, STYLE, RP>(x, r, q_out + v * kD, l, valid && pos_ok);
       store_f32_cs(w_out + v, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold), valid && w_lane);
     };
-    // query heads: warp cw takes head quads cw, cw + kConsumers, ...
-    for (int qd = cw; 4 * qd < n; qd += kConsumers) {
-      float x[16];
-      q_head(4 * qd + qtr, x);
+    if constexpr (HAD) {
+      // query heads in the four-lane layout: lanes 4g .. 4g + 3 take head
+      // 8 qd + g, warp cw the head octets cw, cw + kConsumers, ...
+      const int g = lane >> 2, jj = lane & 3;
+      Rot<RP> r0, r1;  // frequencies 2 RP jj .. 2 RP jj + 2 RP - 1
+      if constexpr (RP > 0) {
+        float cs[2 * RP], sn[2 * RP];
+        load_f32_shared<2 * RP, gcd_pow2(8 * RP)>(sts + kOffCos + 8 * RP * jj, cs);
+        load_f32_shared<2 * RP, gcd_pow2(8 * RP)>(sts + kOffSin + 8 * RP * jj, sn);
+#pragma unroll
+        for (int i = 0; i < RP; ++i) {
+          r0.c[i] = cs[i], r1.c[i] = cs[RP + i];
+          r0.s[i] = sn[i], r1.s[i] = sn[RP + i];
+        }
+        finish_rot<RP>(r0);
+        finish_rot<RP>(r1);
+      }
+      for (int qd = cw; 8 * qd < n; qd += kConsumers) {
+        const int v = 8 * qd + g;
+        const bool valid = v < n;
+        const int vl = valid ? v : n - 1;
+        float x0[16], x1[16];
+        load_hslice_pair<STYLE, RP, SharedMem>(sts + kOffQ + 256 * vl, jj, x0, x1);
+        const float wv = __uint_as_float(static_cast<uint32_t>(w_src[vl]) << 16);
+        if constexpr (RP > 0) {
+          rope_slice<RP>(x0, r0);
+          rope_slice<RP>(x1, r1);
+        }
+        fwht_pair<STYLE, RP>(x0, x1, jj);
+        const int e = exponent_of_amax(__fmul_rn(pair_amax(x0, x1), kHadamardScale));
+        uint32_t w0[4], w1[4];
+        quantize_hslice<STYLE, RP>(x0, e, w0);
+        quantize_hslice<STYLE, RP>(x1, e, w1);
+        store_hslice_pair<STYLE, RP>(q_out + v * kD, jj, w0, w1, valid && pos_ok);
+        store_f32_cs(w_out + v, __fmul_rn(__fmul_rn(wv, pow2f(e)), p.fold),
+                     valid && pos_ok && jj == 0);
+      }
+    } else {
+      // query heads: warp cw takes head quads cw, cw + kConsumers, ...
+      for (int qd = cw; 4 * qd < n; qd += kConsumers) {
+        float x[16];
+        q_head(4 * qd + qtr, x);
+      }
     }
     // the key rides with chunk 0; the warp that takes it rotates per unit
     if (c == 0 && cw == i % kConsumers) {
+      if constexpr (HAD) load_rot8();
       float x[16];
       load_vec<HAD, STYLE, RP, SharedMem>(sts + kOffK, l, x);
       k_slice<HAD, STYLE, RP>(p, x, r, l, qtr == 0, pos_ok, hd->slot);
